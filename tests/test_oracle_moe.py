@@ -1,0 +1,202 @@
+"""Pins of the oracle's norm, router, expert and combine (CPU only).
+
+Checked against hand-worked values (tests/golden/rmsnorm_cases.txt,
+tests/golden/expert_hand_case.txt), closed forms of silu / sigmoid, brute
+force over every k-subset for the top-k, an independent per-element loop for
+the expert contraction, the one-token / one-expert reduction of the whole
+step, and token-permutation invariance.
+"""
+
+import itertools
+import math
+import os
+
+import numpy as np
+
+from oracle import moe
+from oracle.mx import dequant_rows, quant_rows
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rms_cases():
+    out = []
+    with open(os.path.join(GOLDEN, "rmsnorm_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            x, w, eps, want = [p.strip() for p in line.split("|")]
+            out.append((np.array(x.split(), float), np.array(w.split(), float),
+                        float(eps), np.array(want.split(), float)))
+    return out
+
+
+def test_rmsnorm_hand_cases():
+    cases = _rms_cases()
+    assert len(cases) >= 5
+    for x, w, eps, want in cases:
+        got = moe.rmsnorm(x[None, :], w, eps)[0]
+        assert np.array_equal(got, want), (x, w, got, want)
+
+
+def test_silu_sigmoid_closed_forms():
+    assert moe.sigmoid(0.0) == 0.5
+    assert math.isclose(moe.silu(1.0), 0.7310585786300049, rel_tol=1e-15)
+    assert math.isclose(moe.silu(-1.0), -0.2689414213699951, rel_tol=1e-15)
+    assert moe.silu(0.0) == 0.0
+    assert math.isclose(moe.silu(2.0), 1.7615941559557646, rel_tol=1e-15)
+    assert abs(moe.silu(-40.0)) < 1e-15
+
+
+def test_topk_bruteforce():
+    rng = np.random.default_rng(11)
+    for trial in range(200):
+        e = int(rng.integers(2, 11))
+        k = int(rng.integers(1, e + 1))
+        c = rng.standard_normal(e)
+        ids = moe.topk_desc(c[None], k)[0]
+        # the unique k-subset whose every member beats every non-member
+        best = [s for s in itertools.combinations(range(e), k)
+                if min(c[list(s)]) > max(np.delete(c, list(s)), default=-np.inf)]
+        assert len(best) == 1
+        assert sorted(ids.tolist()) == sorted(best[0])
+        assert all(c[ids[j]] > c[ids[j + 1]] for j in range(k - 1))
+
+
+def test_topk_ties_lower_index_first():
+    c = np.array([[1.0, 2.0, 2.0, 0.0, 2.0]])
+    assert moe.topk_desc(c, 2)[0].tolist() == [1, 2]
+    assert moe.topk_desc(c, 4)[0].tolist() == [1, 2, 4, 0]
+
+
+def test_router_hand_case():
+    normed = np.array([[1.0, 0.0]])
+    gate_w = np.array([[0.0, 5.0], [2.0, 1.0], [-1.0, 0.0], [1.0, -3.0]])
+    bias = np.zeros(4)
+    rt = moe.router(normed, gate_w, bias, 2)
+    assert rt.logits.tolist() == [[0.0, 2.0, -1.0, 1.0]]
+    assert rt.ids.tolist() == [[1, 3]]
+    s1, s3 = 0.8807970779778823, 0.7310585786300049  # sigmoid(2), sigmoid(1)
+    assert np.allclose(rt.weights, [[s1 / (s1 + s3), s3 / (s1 + s3)]], rtol=1e-15)
+    # the bias moves the choice but not the weights (scores stay unbiased)
+    rt = moe.router(normed, gate_w, np.array([0.0, 0.0, 0.5, 0.0]), 2)
+    assert rt.ids.tolist() == [[1, 2]]
+    s2 = 0.2689414213699951  # sigmoid(-1)
+    assert np.allclose(rt.weights, [[s1 / (s1 + s2), s2 / (s1 + s2)]], rtol=1e-15)
+
+
+def _hand_expert():
+    h = 32
+    w13 = np.zeros((64, h), np.uint8)
+    w13[:32, 0] = 0x38
+    w13[32 + np.arange(32), np.arange(32)] = 0x38
+    w13_s = np.array([[128], [127]], np.uint8)
+    w2 = np.zeros((h, 32), np.uint8)
+    w2[np.arange(32), np.arange(32)] = 0x38
+    w2_s = np.array([[127]], np.uint8)
+    return w13, w13_s, w2, w2_s
+
+
+def _golden_expert():
+    vals = {}
+    with open(os.path.join(GOLDEN, "expert_hand_case.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = float.fromhex(v) if v.startswith("0x") else float(v)
+    return vals
+
+
+def test_expert_hand_case():
+    g = _golden_expert()
+    ew = moe.ExpertWeights.from_quantised(*_hand_expert())
+    x_hat = dequant_rows(np.full((1, 32), 0x38, np.uint8), np.array([[127]], np.uint8))
+    y, h, hb, hc = moe.expert(x_hat, ew)
+    assert np.allclose(h, g["h"], rtol=1e-15)
+    assert np.all(hc == int(g["h8_code"])) and np.all(hb == int(g["h8_byte"]))
+    assert np.all(y == g["y"])
+
+
+def test_expert_matches_elementwise_loop():
+    # the vectorised expert against a plain triple loop over the dequantised
+    # values, on random small shapes (independent arithmetic path)
+    rng = np.random.default_rng(3)
+    h, inter = 64, 64
+    w13b = rng.integers(0, 0x7E, (2 * inter, h)).astype(np.uint8) | (rng.integers(0, 2, (2 * inter, h)) << 7).astype(np.uint8)
+    w13s = rng.integers(115, 125, (2 * inter // 32, h // 32)).astype(np.uint8)
+    w2b = rng.integers(0, 0x7E, (h, inter)).astype(np.uint8)
+    w2s = rng.integers(110, 120, (h // 32, inter // 32)).astype(np.uint8)
+    ew = moe.ExpertWeights.from_quantised(w13b, w13s, w2b, w2s)
+    x8, xc = quant_rows(rng.standard_normal((1, h)))
+    x_hat = dequant_rows(x8, xc)
+    y, hh, hb, hc = moe.expert(x_hat, ew)
+    from oracle.numerics import e4m3_decode
+    gu = np.zeros(2 * inter)
+    for r in range(2 * inter):
+        acc = 0.0
+        for c in range(h):
+            wv = float(e4m3_decode(w13b[r, c])) * 2.0 ** (int(w13s[r // 32, c // 32]) - 127)
+            xv = float(e4m3_decode(x8[0, c])) * 2.0 ** (int(xc[0, c // 32]) - 127)
+            acc += wv * xv
+        gu[r] = acc
+    href = [gu[i] / (1 + math.exp(-gu[i])) * gu[inter + i] for i in range(inter)]
+    assert np.allclose(hh[0], href, rtol=1e-12, atol=1e-300)
+    hq = dequant_rows(hb, hc)[0]
+    yref = np.zeros(h)
+    for r in range(h):
+        yref[r] = sum(float(e4m3_decode(w2b[r, c])) * 2.0 ** (int(w2s[r // 32, c // 32]) - 127) * hq[c]
+                      for c in range(inter))
+    assert np.allclose(y[0], yref, rtol=1e-12)
+
+
+def _tiny_layer(rng, h=64, e=8, inter=64):
+    def q(shape, code_lo, code_hi):
+        b = rng.integers(0, 0x7E, shape).astype(np.uint8) | (rng.integers(0, 2, shape) << 7).astype(np.uint8)
+        s = rng.integers(code_lo, code_hi, (shape[0] // 32, shape[1] // 32)).astype(np.uint8)
+        return b, s
+    experts = [moe.ExpertWeights.from_quantised(*q((2 * inter, h), 112, 118), *q((h, inter), 112, 118))
+               for _ in range(e)]
+    shared = moe.ExpertWeights.from_quantised(*q((2 * inter, h), 112, 118), *q((h, inter), 112, 118))
+    norm_w = 1 + 0.1 * rng.standard_normal(h)
+    gate_w = 0.1 * rng.standard_normal((e, h))
+    bias = 0.01 * rng.standard_normal(e)
+    return experts, shared, norm_w, gate_w, bias
+
+
+def test_one_token_one_expert_reduction():
+    # k = 1 and a shared expert whose output is zero: out = bf16(y_e) with
+    # weight exactly 1, whatever expert the router picks
+    rng = np.random.default_rng(4)
+    experts, shared, norm_w, gate_w, bias = _tiny_layer(rng)
+    zero = moe.ExpertWeights(w13=shared.w13, w2=np.zeros_like(shared.w2))
+    x = moe.bf16_rne(rng.standard_normal((1, 64)))
+    res = moe.decode_step(x, norm_w, gate_w, bias, 1, lambda e: experts[e], lambda: zero)
+    e = int(res.routing.ids[0, 0])
+    assert res.routing.weights[0, 0] == 1.0
+    y = moe.expert(dequant_rows(res.x8, res.codes), experts[e])[0]
+    assert np.array_equal(res.out, moe.bf16_rne(y))
+
+
+def test_step_token_permutation_invariance():
+    rng = np.random.default_rng(9)
+    experts, shared, norm_w, gate_w, bias = _tiny_layer(rng)
+    x = moe.bf16_rne(rng.standard_normal((5, 64)))
+    perm = np.array([3, 0, 4, 1, 2])
+    a = moe.decode_step(x, norm_w, gate_w, bias, 2, lambda e: experts[e], lambda: shared)
+    b = moe.decode_step(x[perm], norm_w, gate_w, bias, 2, lambda e: experts[e], lambda: shared)
+    assert np.array_equal(a.out[perm], b.out)
+    assert np.array_equal(a.x8[perm], b.x8)
+    assert np.array_equal(a.routing.ids[perm], b.routing.ids)
+
+
+def test_step_token_subset_matches_full():
+    rng = np.random.default_rng(10)
+    experts, shared, norm_w, gate_w, bias = _tiny_layer(rng)
+    x = moe.bf16_rne(rng.standard_normal((4, 64)))
+    full = moe.decode_step(x, norm_w, gate_w, bias, 2, lambda e: experts[e], lambda: shared)
+    part = moe.decode_step(x, norm_w, gate_w, bias, 2, lambda e: experts[e], lambda: shared,
+                           tokens=[2])
+    assert np.array_equal(full.out[2], part.out[2])
+    assert np.all(np.isnan(part.out[[0, 1, 3]]))
