@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Benchmark of the MXFP8 MoE decode step (FFN half) on GB300: one JSON line.
+
+Metric: microseconds per MoE decode step, with the achieved HBM GB/s of the
+dominant kernel against the measured copy bandwidth. A step is one pass of the
+whole path (seam, router, gather, w13 experts, w2 experts, combine) over one
+batch of M synthetic token rows, replayed from a CUDA graph with every input
+resident in HBM; L2 is flushed (a 512 MB write) before every timed step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl mine|reference] [--no-sweep]
+
+--impl reference times the CPU oracle (the reference arm of this build) on a
+bounded sample of the same workload and scales it to one step. Under torchrun
+(N > 1) each rank runs an independent replica of the step (the layer does not
+shard on one box); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per MoE decode step and achieved HBM GB/s (% of 8 TB/s) at M=1..48"
+DEFAULT_WORKLOAD = "full_m48_uniform"
+SWEEP = ["full_m48_zipf", "full_m1", "full_m16", "small_m4"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--cpu-experts", type=int, default=4,
+                    help="experts the CPU baseline evaluates per sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("expert.cu", "ptx.cuh", "mx.cuh", "internal.cuh"):
+        with open(os.path.join(ROOT, "mxfp8_moe_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def make_layer(wl, dev, ew=None):
+    import torch
+
+    from mxfp8_moe_decode_gb300 import MoeDecode
+    from mxfp8_moe_decode_gb300 import workloads as W
+
+    d = wl.dims
+    ri = W.router_inputs(wl)
+    if ew is None:
+        ew = W.expert_weights(wl, device=dev)
+    weights = {"norm_w": ri["norm_w"].to(dev), "gate_w": ri["gate_w"].to(dev),
+               "bias": ri["bias"].to(dev), **ew}
+    layer = MoeDecode(d.hidden, d.experts, d.topk, d.inter, weights, max_tokens=d.max_tokens,
+                      eps=d.eps)
+    x = W.token_rows(wl).to(dev)
+    torch.cuda.synchronize(dev)
+    return layer, x, ew
+
+
+def time_layer(layer, x, dev, steps: int, warmup: int, flush, with_kernel_events=True):
+    """Graph-replay timing: per step flush L2 (untimed), then events around the
+    replay. Returns (per-step ms list, per-kernel mean ms list, unique routed)."""
+    import torch
+
+    from mxfp8_moe_decode_gb300 import kernel_names
+
+    nk = len(kernel_names())
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    if with_kernel_events:
+        layer.set_timing_events(evs)
+    out = torch.empty_like(x)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for _ in range(max(warmup, 3)):
+            layer.step(x, out=out, stream=s)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            layer.step(x, out=out, stream=s)
+    torch.cuda.synchronize(dev)
+    if layer.status() != 0:
+        raise RuntimeError(f"device status {layer.status()}")
+    unique = layer.unique_experts()
+    for _ in range(warmup):
+        flush()
+        g.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms, kern = [], [[] for _ in range(nk)]
+    cur = torch.cuda.current_stream(dev)
+    for _ in range(steps):
+        flush()
+        t0.record(cur)
+        g.replay()
+        t1.record(cur)
+        t1.synchronize()
+        step_ms.append(t0.elapsed_time(t1))
+        if with_kernel_events:
+            for i in range(nk):
+                kern[i].append(evs[i].elapsed_time(evs[i + 1]))
+    torch.cuda.synchronize(dev)
+    layer.set_timing_events(None)
+    if layer.status() != 0:
+        raise RuntimeError(f"device status {layer.status()}")
+    kmean = [statistics.mean(k) if k else None for k in kern]
+    return step_ms, kmean, unique, g, out
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from mxfp8_moe_decode_gb300 import build, kernel_names
+    from mxfp8_moe_decode_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    build.build()
+    wl = W.WORKLOADS[args.workload]
+    d = wl.dims
+    peaks = measured_peaks()
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    layer, x, ew = make_layer(wl, dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with Clocks(local) as clk:
+        step_ms, kmean, unique, graph, out = time_layer(layer, x, dev, args.steps, args.warmup,
+                                                        flush)
+    clocks = clk.summary()
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    us_step = total_ms * 1e3 / (args.steps * world)
+    names = kernel_names()
+    alg = W.algorithmic_bytes(d, unique)
+    i13 = names.index("expert_w13")
+    w13_bytes = (unique + 1) * (2 * d.inter * d.hidden + (2 * d.inter // 32) * (d.hidden // 32))
+    ach = w13_bytes / (kmean[i13] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "expert_w13", "achieved": round(ach, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                "traffic": ncu_traffic("expert_w13"),
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
+                if peaks["source"] == "measured" else "fallback 6.8 TB/s"}
+    step_gbs = alg / (us_step * 1e-6) / 1e9 if world == 1 else None
+
+    # end to end: host (pinned) x -> device, the step, device out -> host
+    xh = x.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    cur = torch.cuda.current_stream(dev)
+    xd = x  # the graph reads x's storage
+    for _ in range(args.warmup):
+        xd.copy_(xh, non_blocking=True)
+        graph.replay()
+        oh.copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e = []
+    for _ in range(args.steps):
+        flush()
+        e0.record(cur)
+        xd.copy_(xh, non_blocking=True)
+        graph.replay()
+        oh.copy_(out, non_blocking=True)
+        e1.record(cur)
+        e1.synchronize()
+        e2e.append(e0.elapsed_time(e1))
+    e2e_us = statistics.mean(e2e) * 1e3
+
+    sweep = {}
+    if not args.no_sweep and world == 1:
+        layer.close()
+        del layer, graph
+        torch.cuda.empty_cache()
+        prev_seed, prev_ew = wl.seed, ew
+        for name in SWEEP:
+            swl = W.WORKLOADS[name]
+            reuse = prev_ew if (swl.seed == prev_seed and swl.dims == d) else None
+            if reuse is None:
+                prev_ew = None
+                torch.cuda.empty_cache()
+            L2, x2, ew2 = make_layer(swl, dev, ew=reuse)
+            ms, km, u2, g2, _ = time_layer(L2, x2, dev, max(5, args.steps // 2), 3, flush)
+            us2 = statistics.mean(ms) * 1e3
+            a2 = W.algorithmic_bytes(swl.dims, u2)
+            i2 = (u2 + 1) * (2 * swl.dims.inter * swl.dims.hidden
+                             + (2 * swl.dims.inter // 32) * (swl.dims.hidden // 32))
+            sweep[name] = {"M": swl.tokens, "us_per_step": round(us2, 2),
+                           "unique_routed": u2, "alg_bytes": a2,
+                           "step_gbs": round(a2 / (us2 * 1e-6) / 1e9, 1),
+                           "step_frac": round(a2 / (us2 * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                           "w13_gbs": round(i2 / (km[i13] * 1e-3) / 1e9, 1),
+                           "kernel_us": {n: round(k * 1e3, 2) for n, k in zip(names, km)}}
+            L2.close()
+            del L2, g2
+            prev_seed, prev_ew = swl.seed, ew2
+
+    line = {
+        "metric": METRIC,
+        "value": round(us_step, 3),
+        "unit": "us",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(us_step / 1e3, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 (mxfp8 block-scaled MMA, fp32 accumulate)",
+        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
+        "config": {"workload": wl.name, "desc": wl.note, "M": wl.tokens, "hidden": d.hidden,
+                   "experts": d.experts, "topk": d.topk, "inter": d.inter,
+                   "shared_experts": 1, "unique_routed_experts": unique,
+                   "alg_bytes_per_step": alg, "step_gbs": round(step_gbs, 1) if step_gbs else None,
+                   "step_frac_of_peak": round(step_gbs / peaks["hbm_gbs"], 4) if step_gbs else None,
+                   "l2": "flushed (512 MB write) before every timed step; weights > L2",
+                   "timing": "CUDA-graph replay, CUDA events per step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "kernel_us": {n: round(k * 1e3, 2) for n, k in zip(names, kmean)},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us",
+                "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2},
+        "gpu_launches": len(names) * args.steps,
+        "clocks": clocks,
+    }
+    if sweep:
+        line["sweep"] = sweep
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_experts, unique)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- CPU oracle
+_CPU_WEIGHTS: dict = {}
+
+
+def cpu_baseline(wl, n_experts: int, unique: int | None = None, repeats: int = 1) -> dict:
+    """The oracle, as it stands, on the host cores: the seam and router on all M
+    rows plus the expert path of a sample of the touched experts (dequantise +
+    per-token contraction), scaled to the step's unique + shared experts."""
+    import numpy as np
+    import torch
+
+    from mxfp8_moe_decode_gb300 import workloads as W
+    from oracle import moe as O
+    from oracle.mx import dequant_rows
+
+    d = wl.dims
+    ri = W.router_inputs(wl)
+    x = W.token_rows(wl)
+    f64 = lambda t: t.float().double().numpy()  # noqa: E731
+    t0 = time.perf_counter()
+    normed = O.rmsnorm(f64(x), f64(ri["norm_w"]), d.eps)
+    x8, codes = O.seam_quant(normed)
+    rt = O.router(normed, f64(ri["gate_w"]), f64(ri["bias"]), d.topk)
+    x_hat = dequant_rows(x8, codes)
+    t_front = time.perf_counter() - t0
+    ids = np.unique(rt.ids)
+    u = len(ids) if unique is None else unique
+    sample = [int(e) for e in ids[:n_experts]]
+    key = (wl.name, tuple(sample))
+    if key not in _CPU_WEIGHTS:
+        _CPU_WEIGHTS.clear()
+        _CPU_WEIGHTS[key] = W.expert_weights(wl, device="cpu", experts=sample)
+    ew = _CPU_WEIGHTS[key]
+    t_exp = 0.0
+    for e in sample:
+        tok = [t for t in range(x.shape[0]) if e in rt.ids[t]]
+        t1 = time.perf_counter()
+        w = O.ExpertWeights.from_quantised(ew["w13"][e].numpy(), ew["w13_s"][e].numpy(),
+                                           ew["w2"][e].numpy(), ew["w2_s"][e].numpy())
+        O.expert(x_hat[tok], w)
+        t_exp += time.perf_counter() - t1
+    per_expert = t_exp / max(1, len(sample))
+    est_s = t_front + per_expert * (u + 1)
+    return {"value": round(est_s * 1e6, 1), "unit": "us", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{wl.name}: seam + router on all {x.shape[0]} rows, then the fp64 expert "
+                      f"path of {len(sample)} of the {u} touched routed experts "
+                      f"({per_expert:.2f} s each), scaled to {u} + 1 shared experts"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from mxfp8_moe_decode_gb300 import workloads as W
+
+    wl = W.WORKLOADS[args.workload]
+    vals = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        info = cpu_baseline(wl, 1)
+        if i >= args.warmup:
+            vals.append(info["value"])
+    v = statistics.mean(vals)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(v, 1),
+        "unit": "us",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(v / 1e3, 3),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "desc": wl.note, "M": wl.tokens},
+        "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": info["cores"],
+                         "kind": "oracle", "sample": info["sample"]},
+        "e2e": {"value": round(v, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+/*
+ * moe_decode.h -- C ABI of the GB300 (sm_103a) MXFP8 MoE decode step.
+ *
+ * One call computes the FFN half of one MoE decode step for M <= max_tokens
+ * token rows, on one GPU, unsharded:
+ *
+ *   normed = bf16(RMSNorm(x) * norm_w)                      (FFN seam)
+ *   x8, c  = MXFP8(normed): E4M3 bytes + one E8M0 code / 32  (seam quant)
+ *   s      = sigmoid(normed . gate_w^T); ids = top-k(s + bias); w = s[ids]/sum
+ *   y_e    = MX-GEMM(requant(silu(g) * u), w2_e),  [g; u] = MX-GEMM(x8, w13_e)
+ *   out    = bf16(sum_j w_j * y_{ids_j} + y_shared)
+ *
+ * Sources (the pages this library restates):
+ *  - "vllm.models.deepseek_v41.amd.mono.runner": DSV41MonoLayer.ffn (one launch
+ *    from the FFN seam to the MoE output; every argument a device pointer so
+ *    the launch can be captured in a graph), DSV41MonoLayer.supports
+ *    (1 <= tokens <= MAX_TOKENS = 48), DSV41MonoLayer.scratch (scratch
+ *    allocated up front, never inside a capture), MonoLayerWeights and its
+ *    check (tensor shapes: gate_w [E, 5120] bf16, bias [E] f32, shared
+ *    gate_up [2 inter, 5120] e4m3 with [2 inter/32, 160] E8M0, shared down
+ *    [5120, inter] e4m3 with [160, inter/32]), _check_tensors (shape / dtype /
+ *    contiguity are validated because the kernels' loads are unbounded).
+ *  - "vllm.models.deepseek_v41.amd.mono.layer": run_ffn (stage order: norm ->
+ *    bf16 MoE input row -> MoE), store_normed, store_x8 (MXFP8 of 32-groups).
+ *  - "vllm.models.deepseek_v41.amd.mono.attention.device": mx_code, ceil_exp,
+ *    div_rn, mx_mul, fp8_pack4 (E4M3 RNE), mfma_scaled (block-scaled MMA).
+ *
+ * Conventions shared by every entry point:
+ *  - Return value: MOE_OK (0) or a negative MOE_ERR_* code; nothing throws.
+ *  - Pointers named "device" are CUDA device pointers on the handle's device;
+ *    "host" pointers are ordinary process memory.
+ *  - Ownership: the caller owns every buffer it passes (weights, inputs,
+ *    outputs, debug buffers) and keeps the weights alive and unchanged for the
+ *    lifetime of the handle. The library owns its scratch and frees it in
+ *    moe_destroy.
+ *  - Streams are passed as void* holding a cudaStream_t (NULL = the legacy
+ *    default stream).
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define MOE_OK 0
+#define MOE_ERR_ARG (-1)         /* null or inconsistent argument */
+#define MOE_ERR_RANGE (-2)       /* M outside [1, max_tokens] */
+#define MOE_ERR_ALIGN (-3)       /* a device pointer is not 16-byte aligned */
+#define MOE_ERR_CUDA (-4)        /* a CUDA runtime / driver call failed */
+#define MOE_ERR_CAPTURE (-5)     /* not allowed while the stream is being captured */
+#define MOE_ERR_TIMEOUT (-6)     /* a bounded device-side wait expired (moe_status) */
+#define MOE_ERR_UNSUPPORTED (-7) /* configuration outside what the kernels implement */
+#define MOE_ERR_DEVICE (-8)      /* the device is not a compute capability 10.3 GPU */
+
+/*
+ * Layer dimensions.
+ *  hidden        H: multiple of 128, 256..8192.
+ *  experts       E: routed experts, multiple of 32, 32..512.
+ *  topk          k: 1..16 and <= E.
+ *  inter         I: routed expert intermediate size, multiple of 128.
+ *  shared_inter  the shared expert's intermediate size; must equal inter.
+ *  max_tokens    largest M a step may use, 1..48 (the pages' MAX_TOKENS).
+ *  eps           RMSNorm epsilon (1e-6 for the pages' layer).
+ */
+typedef struct moe_config {
+  int hidden;
+  int experts;
+  int topk;
+  int inter;
+  int shared_inter;
+  int max_tokens;
+  float eps;
+} moe_config;
+
+/*
+ * Weights: device pointers, row-major, contiguous, 16-byte aligned, read by
+ * every step (the E8M0 weight scales are also packed once by moe_create into
+ * the kernels' tile order, so changing them later needs a new handle).
+ *  norm_w  bf16 [H]                      RMSNorm weight, used as given
+ *  gate_w  bf16 [E, H]                   router gate
+ *  bias    f32  [E]                      e_score_correction_bias (selection only)
+ *  w13     e4m3 [E, 2I, H]               rows [0, I) gate, rows [I, 2I) up
+ *  w13_s   u8   [E, 2I/32, H/32]         E8M0 code of each 32 x 32 block
+ *  w2      e4m3 [E, H, I]                down projection
+ *  w2_s    u8   [E, H/32, I/32]
+ *  sw13, sw13_s, sw2, sw2_s              the shared expert, same layouts
+ *                                        without the E axis
+ */
+typedef struct moe_weights {
+  const void* norm_w;
+  const void* gate_w;
+  const float* bias;
+  const uint8_t* w13;
+  const uint8_t* w13_s;
+  const uint8_t* w2;
+  const uint8_t* w2_s;
+  const uint8_t* sw13;
+  const uint8_t* sw13_s;
+  const uint8_t* sw2;
+  const uint8_t* sw2_s;
+} moe_weights;
+
+/*
+ * Optional per-step outputs for checking the intermediate steps (device
+ * pointers; any may be NULL; each must hold M rows of the given width):
+ *  normed    bf16 [M, H]     the MoE input row (FFN seam output)
+ *  x8        u8   [M, H]     its E4M3 bytes
+ *  x8_codes  u8   [M, H/32]  its E8M0 codes
+ *  topk_ids  i32  [M, k]     chosen experts, decreasing score + bias
+ *  topk_w    f32  [M, k]     their normalised weights
+ *  logits    f32  [M, E]     router logits
+ */
+typedef struct moe_debug {
+  void* normed;
+  uint8_t* x8;
+  uint8_t* x8_codes;
+  int32_t* topk_ids;
+  float* topk_w;
+  float* logits;
+} moe_debug;
+
+typedef struct moe_handle moe_handle;
+
+/*
+ * Validates cfg and the weight pointers, makes `device` current, allocates the
+ * step's scratch for cfg->max_tokens rows (all of it, up front), packs the
+ * weight scales, encodes the TMA descriptors, and synchronises the device.
+ * On success *out holds a new handle. Errors: MOE_ERR_ARG (null / bad dims),
+ * MOE_ERR_UNSUPPORTED (dims outside the limits above), MOE_ERR_ALIGN,
+ * MOE_ERR_DEVICE, MOE_ERR_CUDA, MOE_ERR_CAPTURE (the legacy stream of
+ * `device` is being captured: creation allocates and synchronises).
+ */
+int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_handle** out);
+
+/*
+ * Enqueues one decode step on `stream` (the handle's device must be current):
+ * x bf16 [M, H] device -> out bf16 [M, H] device (the MoE output only; no
+ * residual is added). Kernel launches only: no allocation, no host
+ * synchronisation, so the call may be captured into a CUDA graph. Steps on
+ * one handle share its scratch, so they must not run concurrently (enqueue
+ * them on one stream). Errors are checked before anything is enqueued:
+ * MOE_ERR_RANGE (M < 1 or M > max_tokens), MOE_ERR_ARG, MOE_ERR_ALIGN,
+ * MOE_ERR_CUDA (a launch failed). A device-side failure (a bounded wait that
+ * expired) is reported later by moe_status.
+ */
+int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream,
+                    const moe_debug* dbg);
+
+/*
+ * Synchronises the handle's device and returns MOE_OK, MOE_ERR_TIMEOUT if a
+ * step's kernel gave up a bounded wait since the last moe_clear_status, or
+ * MOE_ERR_CUDA if the device reported an error. Not allowed during capture
+ * (MOE_ERR_CAPTURE).
+ */
+int moe_status(moe_handle* h);
+
+/* Resets the device-side error word (synchronous). MOE_ERR_CAPTURE during capture. */
+int moe_clear_status(moe_handle* h);
+
+/*
+ * Number of distinct routed experts the last completed step used (synchronous
+ * read of the device routing table into *unique_routed). For byte accounting.
+ */
+int moe_last_unique_experts(moe_handle* h, int* unique_routed);
+
+/*
+ * Timing hooks for profiling: while set, every step records events[i]
+ * (cudaEvent_t values, caller-owned) on its stream just before kernel i and
+ * events[n_kernels] after the last kernel; n must equal moe_kernel_count()+1.
+ * Pass events = NULL, n = 0 to turn it off.
+ */
+int moe_set_timing_events(moe_handle* h, void* const* events, int n);
+
+/* Number of kernels one step launches, and the name of kernel i (static string). */
+int moe_kernel_count(void);
+const char* moe_kernel_name(int i);
+
+/*
+ * Diagnostics: device address and size of one region of the handle's scratch,
+ * valid until moe_destroy; contents are those of the last completed step.
+ * Regions (layouts are internal and may change):
+ *  MOE_REGION_GATHERED  u8  [rows][H]  MXFP8 token rows grouped by active expert
+ *  MOE_REGION_H8        u8  [rows][I]  requantised silu(g) * u rows, same order
+ *  MOE_REGION_PARTIAL   f32 [rows][H]  expert output rows y, same order
+ *  MOE_REGION_ACTIVE    i32 [E + 1][4] active experts: expert, first row, rows, 0
+ *  MOE_REGION_TOKPOS    i32 [M][k + 1] row of (token, pick); pick k = shared expert
+ * rows = M * (k + 1) for the step's M: the routed picks first (experts in
+ * increasing id, tokens in increasing index), then the shared expert's M rows.
+ */
+#define MOE_REGION_GATHERED 0
+#define MOE_REGION_H8 1
+#define MOE_REGION_PARTIAL 2
+#define MOE_REGION_ACTIVE 3
+#define MOE_REGION_TOKPOS 4
+int moe_scratch_region(const moe_handle* h, int region, void** ptr, size_t* bytes);
+
+/* Bytes of device scratch the handle holds. */
+size_t moe_scratch_bytes(const moe_handle* h);
+
+/* Static description of an error code. */
+const char* moe_strerror(int code);
+
+/* Frees the handle's scratch and the handle (NULL is allowed). */
+void moe_destroy(moe_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_H */

@@ -1,0 +1,497 @@
+// The C ABI (include/moe_decode.h): handle creation with the whole scratch
+// allocated up front, the step as a fixed sequence of kernel launches on the
+// caller's stream, and the status / timing helpers.
+//
+// "vllm.models.deepseek_v41.amd.mono.runner": DSV41MonoLayer.ffn (the step),
+// supports (1 <= M <= MAX_TOKENS), scratch (allocated before any capture;
+// here all widths share one scratch sized for max_tokens), _check_tensors
+// (inputs are validated because the kernels' loads are unbounded).
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.cuh"
+
+using namespace moe;
+
+struct moe_handle {
+  moe_config cfg;
+  moe_weights w;
+  int device;
+  int num_sms;
+  int ks, hs;
+  int units_max, rows_max, rows_alloc;
+  uint8_t* scratch;
+  size_t scratch_bytes;
+  int* counters;
+  ActiveExpert* act;
+  float* route_w;
+  int* tok_pos;
+  int* pos_tok;
+  __nv_bfloat16* normed;
+  uint8_t* x8;
+  uint8_t* x8c;
+  float* logit_part;
+  uint8_t* xg;
+  uint8_t* h8;
+  uint4* sfb13;
+  uint8_t* sfb2;
+  float* part;
+  uint4* sfa13;
+  uint4* sfa2;
+  ExpertParams p13;
+  ExpertParams p2;
+  cudaEvent_t events[16];
+  int n_events;
+  cudaStream_t last_stream;
+};
+
+namespace {
+
+const char* const kKernelNames[] = {"seam", "router", "gather", "expert_w13", "expert_w2",
+                                    "combine"};
+constexpr int kNumKernels = 6;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int cuda_code(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  if (e == cudaErrorStreamCaptureUnsupported || e == cudaErrorStreamCaptureInvalidated ||
+      e == cudaErrorStreamCaptureImplicit || e == cudaErrorStreamCaptureWrongThread)
+    return MOE_ERR_CAPTURE;
+  return MOE_ERR_CUDA;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2D uint8 matrix [rows][cols] (row stride = cols bytes), box = 128 bytes x box_rows,
+// 128-byte swizzle (the layout the MMA's shared-memory descriptors describe).
+bool encode_rows(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
+                 uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int validate_config(const moe_config* c) {
+  if (c->hidden <= 0 || c->experts <= 0 || c->topk <= 0 || c->inter <= 0 ||
+      c->shared_inter <= 0 || c->max_tokens <= 0 || !(c->eps >= 0.0f))
+    return MOE_ERR_ARG;
+  if (c->hidden % 128 || c->hidden < 256 || c->hidden > 8192) return MOE_ERR_UNSUPPORTED;
+  if (c->experts % 32 || c->experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (c->topk > kMaxTopk || c->topk > c->experts) return MOE_ERR_UNSUPPORTED;
+  if (c->inter % 128 || c->shared_inter != c->inter) return MOE_ERR_UNSUPPORTED;
+  if (c->max_tokens > kMaxTokens) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int validate_weights(const moe_weights* w) {
+  const void* ptrs[] = {w->norm_w, w->gate_w, w->bias, w->w13, w->w13_s, w->w2,
+                        w->w2_s,   w->sw13,   w->sw13_s, w->sw2, w->sw2_s};
+  for (const void* p : ptrs) {
+    if (!p) return MOE_ERR_ARG;
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_kernel_count(void) { return kNumKernels; }
+
+const char* moe_kernel_name(int i) {
+  return (i >= 0 && i < kNumKernels) ? kKernelNames[i] : nullptr;
+}
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_RANGE: return "token count outside [1, max_tokens]";
+    case MOE_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_CAPTURE: return "not allowed during stream capture";
+    case MOE_ERR_TIMEOUT: return "a bounded device wait expired";
+    case MOE_ERR_UNSUPPORTED: return "configuration not supported";
+    case MOE_ERR_DEVICE: return "device is not compute capability 10.3";
+    default: return "unknown error";
+  }
+}
+
+size_t moe_scratch_bytes(const moe_handle* h) { return h ? h->scratch_bytes : 0; }
+
+int moe_scratch_region(const moe_handle* h, int region, void** ptr, size_t* bytes) {
+  if (!h || !ptr || !bytes) return MOE_ERR_ARG;
+  const size_t H = h->cfg.hidden, I = h->cfg.inter, K = h->cfg.topk;
+  switch (region) {
+    case MOE_REGION_GATHERED:
+      *ptr = h->xg;
+      *bytes = static_cast<size_t>(h->rows_max) * H;
+      return MOE_OK;
+    case MOE_REGION_H8:
+      *ptr = h->h8;
+      *bytes = static_cast<size_t>(h->rows_max) * I;
+      return MOE_OK;
+    case MOE_REGION_PARTIAL:
+      *ptr = h->part;
+      *bytes = static_cast<size_t>(h->rows_max) * H * 4;
+      return MOE_OK;
+    case MOE_REGION_ACTIVE:
+      *ptr = h->act;
+      *bytes = static_cast<size_t>(h->cfg.experts + 1) * sizeof(ActiveExpert);
+      return MOE_OK;
+    case MOE_REGION_TOKPOS:
+      *ptr = h->tok_pos;
+      *bytes = static_cast<size_t>(h->cfg.max_tokens) * (K + 1) * 4;
+      return MOE_OK;
+    default:
+      return MOE_ERR_ARG;
+  }
+}
+
+int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_handle** out) {
+  if (!cfg || !w || !out) return MOE_ERR_ARG;
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  rc = validate_weights(w);
+  if (rc) return rc;
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return ndev == 0 ? MOE_ERR_CUDA : MOE_ERR_ARG;
+  }
+  if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return MOE_ERR_DEVICE;
+  if (!get_encode_fn()) return MOE_ERR_CUDA;
+
+  moe_handle* h = new (std::nothrow) moe_handle();
+  if (!h) return MOE_ERR_CUDA;
+  std::memset(h, 0, sizeof(*h));
+  h->cfg = *cfg;
+  h->w = *w;
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+
+  const int H = cfg->hidden, E = cfg->experts, K = cfg->topk, I = cfg->inter;
+  const int Mx = cfg->max_tokens;
+  // router K-split: about 128 CTAs, each slice <= 2048 columns, a multiple of 8
+  int ks = 128 / (E / kRouterWarps);
+  if (ks < 1) ks = 1;
+  if (ks > 16) ks = 16;
+  while (H / ks > 2048) ks *= 2;
+  while (H % (ks * 8)) ks /= 2;
+  h->ks = ks;
+  h->hs = H / ks;
+  h->rows_max = Mx * (K + 1);
+  h->rows_alloc = h->rows_max + kMaxTokens;
+  h->units_max = (E < Mx * K ? E : Mx * K) + 1;
+  const int g13 = H / 128, g2 = I / 128, t13 = I / 64, t2 = H / 128;
+
+  size_t off = 0;
+  auto place = [&](size_t bytes) {
+    const size_t o = off;
+    off += round_up(bytes, 1024);
+    return o;
+  };
+  const size_t o_ctr = place(kCtrWords * 4);
+  const size_t o_act = place(static_cast<size_t>(E + 1) * sizeof(ActiveExpert));
+  const size_t o_rw = place(static_cast<size_t>(Mx) * K * 4);
+  const size_t o_tp = place(static_cast<size_t>(Mx) * (K + 1) * 4);
+  const size_t o_pt = place(static_cast<size_t>(h->rows_max) * 4);
+  const size_t o_nm = place(static_cast<size_t>(Mx) * H * 2);
+  const size_t o_x8 = place(static_cast<size_t>(Mx) * H);
+  const size_t o_x8c = place(static_cast<size_t>(Mx) * H / 32);
+  const size_t o_lp = place(static_cast<size_t>(ks) * Mx * E * 4);
+  const size_t o_xg = place(static_cast<size_t>(h->rows_alloc) * H);
+  const size_t o_h8 = place(static_cast<size_t>(h->rows_alloc) * I);
+  const size_t o_s13 = place(static_cast<size_t>(h->units_max) * g13 * 512);
+  const size_t o_s2 = place(static_cast<size_t>(h->units_max) * g2 * 512);
+  const size_t o_pa = place(static_cast<size_t>(h->rows_max) * H * 4);
+  const size_t o_a13 = place(static_cast<size_t>(E + 1) * t13 * g13 * 16);
+  const size_t o_a2 = place(static_cast<size_t>(E + 1) * t2 * g2 * 16);
+  h->scratch_bytes = off;
+
+  cudaError_t err = cudaMalloc(&h->scratch, h->scratch_bytes);
+  if (err != cudaSuccess) {
+    rc = cuda_code(err);
+    cudaGetLastError();
+    delete h;
+    return rc;
+  }
+  uint8_t* b = h->scratch;
+  h->counters = reinterpret_cast<int*>(b + o_ctr);
+  h->act = reinterpret_cast<ActiveExpert*>(b + o_act);
+  h->route_w = reinterpret_cast<float*>(b + o_rw);
+  h->tok_pos = reinterpret_cast<int*>(b + o_tp);
+  h->pos_tok = reinterpret_cast<int*>(b + o_pt);
+  h->normed = reinterpret_cast<__nv_bfloat16*>(b + o_nm);
+  h->x8 = b + o_x8;
+  h->x8c = b + o_x8c;
+  h->logit_part = reinterpret_cast<float*>(b + o_lp);
+  h->xg = b + o_xg;
+  h->h8 = b + o_h8;
+  h->sfb13 = reinterpret_cast<uint4*>(b + o_s13);
+  h->sfb2 = b + o_s2;
+  h->part = reinterpret_cast<float*>(b + o_pa);
+  h->sfa13 = reinterpret_cast<uint4*>(b + o_a13);
+  h->sfa2 = reinterpret_cast<uint4*>(b + o_a2);
+
+  err = cudaMemset(h->scratch, 0, h->scratch_bytes);
+  if (err == cudaSuccess) err = router_setup();
+  if (err == cudaSuccess) err = expert_kernel_setup();
+  if (err == cudaSuccess) {
+    SfaPackParams sp;
+    sp.w13_s = w->w13_s;
+    sp.sw13_s = w->sw13_s;
+    sp.w2_s = w->w2_s;
+    sp.sw2_s = w->sw2_s;
+    sp.sfa13 = h->sfa13;
+    sp.sfa2 = h->sfa2;
+    sp.E = E;
+    sp.H = H;
+    sp.I = I;
+    err = launch_sfa_pack(sp, 0);
+  }
+  if (err == cudaSuccess) err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) {
+    rc = cuda_code(err);
+    cudaGetLastError();
+    cudaFree(h->scratch);
+    delete h;
+    return rc;
+  }
+
+  // expert kernel parameter blocks (fixed for the handle's lifetime)
+  ExpertParams* ps[2] = {&h->p13, &h->p2};
+  for (ExpertParams* p : ps) {
+    p->counters = h->counters;
+    p->act = h->act;
+    p->err = h->counters + kCtrErr;
+    p->E = E;
+    p->inter = I;
+    p->hidden = H;
+    p->units_max = h->units_max;
+    p->rows_max = h->rows_max;
+  }
+  h->p13.sfa = h->sfa13;
+  h->p13.sfb = reinterpret_cast<const uint8_t*>(h->sfb13);
+  h->p13.h8 = h->h8;
+  h->p13.sfb_next = h->sfb2;
+  h->p13.part = nullptr;
+  h->p13.tiles = t13;
+  h->p13.G = g13;
+  h->p13.a_rows = 2 * I;
+  h->p13.next_G = g2;
+  h->p2.sfa = h->sfa2;
+  h->p2.sfb = h->sfb2;
+  h->p2.h8 = nullptr;
+  h->p2.sfb_next = nullptr;
+  h->p2.part = h->part;
+  h->p2.tiles = t2;
+  h->p2.G = g2;
+  h->p2.a_rows = H;
+  h->p2.next_G = 0;
+  bool ok = encode_rows(&h->p13.tm_a, w->w13, H, static_cast<uint64_t>(E) * 2 * I, 64) &&
+            encode_rows(&h->p13.tm_a_shared, w->sw13, H, 2ull * I, 64) &&
+            encode_rows(&h->p13.tm_b, h->xg, H, h->rows_alloc, kBoxRows) &&
+            encode_rows(&h->p2.tm_a, w->w2, I, static_cast<uint64_t>(E) * H, kTileM) &&
+            encode_rows(&h->p2.tm_a_shared, w->sw2, I, static_cast<uint64_t>(H), kTileM) &&
+            encode_rows(&h->p2.tm_b, h->h8, I, h->rows_alloc, kBoxRows);
+  if (!ok) {
+    cudaFree(h->scratch);
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream,
+                    const moe_debug* dbg) {
+  if (!h) return MOE_ERR_ARG;
+  if (M < 1 || M > h->cfg.max_tokens) return MOE_ERR_RANGE;
+  if (!x || !out) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(out)) return MOE_ERR_ALIGN;
+  moe_debug d;
+  std::memset(&d, 0, sizeof(d));
+  if (dbg) d = *dbg;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_stream = st;
+  const int H = h->cfg.hidden, E = h->cfg.experts, K = h->cfg.topk;
+  const bool timed = h->n_events == kNumKernels + 1;
+  cudaError_t err = cudaSuccess;
+  auto mark = [&](int i) {
+    if (timed && err == cudaSuccess) err = cudaEventRecord(h->events[i], st);
+  };
+
+  SeamParams sp;
+  sp.x = static_cast<const __nv_bfloat16*>(x);
+  sp.norm_w = static_cast<const __nv_bfloat16*>(h->w.norm_w);
+  sp.normed = h->normed;
+  sp.x8 = h->x8;
+  sp.x8c = h->x8c;
+  sp.dbg_normed = static_cast<__nv_bfloat16*>(d.normed);
+  sp.dbg_x8 = d.x8;
+  sp.dbg_x8c = d.x8_codes;
+  sp.H = H;
+  sp.eps = h->cfg.eps;
+
+  RouterParams rp;
+  rp.normed = h->normed;
+  rp.gate_w = static_cast<const __nv_bfloat16*>(h->w.gate_w);
+  rp.bias = h->w.bias;
+  rp.logit_part = h->logit_part;
+  rp.counters = h->counters;
+  rp.act = h->act;
+  rp.route_w = h->route_w;
+  rp.tok_pos = h->tok_pos;
+  rp.pos_tok = h->pos_tok;
+  rp.dbg_ids = d.topk_ids;
+  rp.dbg_w = d.topk_w;
+  rp.dbg_logits = d.logits;
+  rp.M = M;
+  rp.H = H;
+  rp.E = E;
+  rp.K = K;
+  rp.KS = h->ks;
+  rp.Hs = h->hs;
+
+  GatherParams gp;
+  gp.x8 = h->x8;
+  gp.x8c = h->x8c;
+  gp.counters = h->counters;
+  gp.act = h->act;
+  gp.pos_tok = h->pos_tok;
+  gp.xg = h->xg;
+  gp.sfb13 = h->sfb13;
+  gp.M = M;
+  gp.H = H;
+  gp.K = K;
+  gp.G = H / 128;
+  gp.units_max = h->units_max;
+  gp.rows_max = h->rows_max;
+
+  CombineParams cp;
+  cp.part = h->part;
+  cp.route_w = h->route_w;
+  cp.tok_pos = h->tok_pos;
+  cp.out = static_cast<__nv_bfloat16*>(out);
+  cp.M = M;
+  cp.H = H;
+  cp.K = K;
+
+  mark(0);
+  if (err == cudaSuccess) err = launch_seam(sp, M, st);
+  mark(1);
+  if (err == cudaSuccess) err = launch_router(rp, st);
+  mark(2);
+  if (err == cudaSuccess) err = launch_gather(gp, h->num_sms, st);
+  mark(3);
+  if (err == cudaSuccess) err = launch_expert13(h->p13, h->num_sms, st);
+  mark(4);
+  if (err == cudaSuccess) err = launch_expert2(h->p2, h->num_sms, st);
+  mark(5);
+  if (err == cudaSuccess) err = launch_combine(cp, st);
+  mark(6);
+  return cuda_code(err);
+}
+
+int moe_status(moe_handle* h) {
+  if (!h) return MOE_ERR_ARG;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(h->last_stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CAPTURE;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return MOE_ERR_CAPTURE;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, h->counters + kCtrErr, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (word & kErrBounds) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+int moe_clear_status(moe_handle* h) {
+  if (!h) return MOE_ERR_ARG;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(h->last_stream, &cs) != cudaSuccess ||
+      cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return MOE_ERR_CAPTURE;
+  }
+  if (cudaSetDevice(h->device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(h->counters + kCtrErr, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaDeviceSynchronize() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_last_unique_experts(moe_handle* h, int* unique_routed) {
+  if (!h || !unique_routed) return MOE_ERR_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, h->counters + kCtrRouted, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *unique_routed = v;
+  return MOE_OK;
+}
+
+int moe_set_timing_events(moe_handle* h, void* const* events, int n) {
+  if (!h) return MOE_ERR_ARG;
+  if (!events || n == 0) {
+    h->n_events = 0;
+    return MOE_OK;
+  }
+  if (n != kNumKernels + 1) return MOE_ERR_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (!events[i]) return MOE_ERR_ARG;
+    h->events[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  h->n_events = n;
+  return MOE_OK;
+}
+
+void moe_destroy(moe_handle* h) {
+  if (!h) return;
+  if (cudaSetDevice(h->device) == cudaSuccess) {
+    cudaDeviceSynchronize();
+    cudaFree(h->scratch);
+  }
+  cudaGetLastError();
+  delete h;
+}
+
+}  // extern "C"

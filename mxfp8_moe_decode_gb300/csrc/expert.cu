@@ -1,0 +1,360 @@
+// Grouped-expert kernel: block-scaled E4M3 GEMMs of the active experts on the
+// 5th-generation tensor cores (tcgen05, accumulators in TMEM), persistent over
+// the step's (expert, weight-tile) tasks.
+//
+// "vllm.models.deepseek_v41.amd.mono.attention.device", mfma_scaled: the
+// expert GEMMs are block-scaled MMAs whose operands are both MX-FP8 with one
+// E8M0 per 32-K block per row. "vllm.models.deepseek_v41.amd.mono.runner",
+// MonoLayerWeights: gate_up [2 inter, 5120] e4m3 with [2 inter / 32, 160]
+// E8M0 (32 x 32 blocks), down [5120, inter] with [160, inter / 32].
+//
+// Swap-AB: the weight rows are the MMA's M (128 per tile) and the expert's
+// tokens its N (rounded up to 16, at most 48), so the weights stream once
+// through shared memory while the few activation rows are reused from L2.
+//
+//  PHASE 13  task = (expert, 64 intermediate columns): A = the 64 gate rows
+//            over the matching 64 up rows of w13 (two TMA boxes), B = the
+//            expert's gathered MXFP8 token rows, K = H. Epilogue: silu(g) * u,
+//            requantised per token in 32-column groups (the same mx_code / E4M3
+//            rule as the seam) into h8 rows and the E8M0 images of the w2 pass.
+//  PHASE 2   task = (expert, 128 hidden rows): A = w2 rows, B = the expert's
+//            h8 rows, K = I. Epilogue: fp32 rows of y for the combine.
+//
+// Per CTA (one per SM, 256 threads): warp 0 lane 0 issues the TMA loads into
+// an 8-stage ring (weights evict-first from L2; activations, scale entries and
+// scale images by TMA / bulk copies); warp 1 expands each stage's 16-byte
+// weight-scale entry into the 32 x 16-byte image tcgen05.cp expects, copies
+// both scale images into TMEM and issues 4 MMAs (K = 32 each, the descriptor's
+// scale-factor id picks the K block of the stage); warp 2 owns the TMEM
+// allocation; warps 4-7 drain the double-buffered accumulator (each reads its
+// 32-lane quarter). Every mbarrier wait is bounded; on a timeout the CTA
+// records kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
+#include "internal.cuh"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr uint32_t kABytes = kTileM * kStageK;           // 16 KB
+constexpr uint32_t kBBytes = kMaxTokens * kStageK;       // 6 KB
+constexpr uint32_t kImgBytes = 32 * 16;                  // scale image of one stage
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kImgBytes;
+constexpr uint32_t kOffSfac = kOffSfb + kStages * kImgBytes;
+constexpr uint32_t kOffXchg = kOffSfac + kStages * 16;
+constexpr uint32_t kOffBar = kOffXchg + kMaxTokens * 64 * 4;
+constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kSmemUsed = kOffMisc + 64;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
+constexpr uint32_t kTmemCols = 256;  // 2 accumulators x 64 + 8 stages x 8 scale columns
+constexpr uint32_t kAccCols = 64;
+constexpr uint32_t kSfCol0 = 128;
+
+static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "B tiles must stay 1024-aligned");
+static_assert(kOffSfa % 512 == 0, "scale images alignment");
+static_assert(kSfCol0 + kStages * 8 <= kTmemCols, "TMEM budget");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+struct Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+};
+static_assert(sizeof(Bars) <= 256, "barrier area");
+
+struct Misc {
+  uint32_t tmem_base;
+  int abort;
+  int epi_ok;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ bool task_valid(const int4& a, const ExpertParams& p) {
+  return a.x >= 0 && a.x <= p.E && a.z >= 1 && a.z <= kMaxTokens && a.y >= 0 &&
+         a.y + a.z <= p.rows_max;
+}
+
+// Lane 0 waits, the warp agrees on the outcome, then every lane observes the
+// completed phase itself (returns at once) so its later reads are ordered.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = ptx::mbar_wait(bar, parity, abort, kWaitLimitNs);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok && (threadIdx.x & 31) != 0) ptx::mbar_wait(bar, parity, abort, kWaitLimitNs);
+  return ok != 0;
+}
+
+// Wait used only while shutting down: bounded by time, ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  int never = 0;
+  ptx::mbar_wait(bar, parity, &never, kWaitLimitNs);
+}
+
+template <int PHASE>
+__global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_constant__ ExpertParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+  volatile int* abort = &misc->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_u32(&bars->tfull[a]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->tempty[a]), 4);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    misc->abort = 0;
+    misc->epi_ok = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&p.tm_a);
+    ptx::prefetch_tmap(&p.tm_a_shared);
+    ptx::prefetch_tmap(&p.tm_b);
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc(ptx::smem_u32(&misc->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tbase = misc->tmem_base;
+
+  int units = p.counters[kCtrUnits];
+  if (units < 0 || units > p.units_max) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
+    units = 0;
+  }
+  const int ntasks = units * p.tiles;
+  const int G = p.G;
+  const int4* act = reinterpret_cast<const int4*>(p.act);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
+        const int u = task / p.tiles, t = task - u * p.tiles;
+        const int4 a = act[u];
+        if (!task_valid(a, p)) continue;
+        const int nt = (a.z + 15) & ~15;
+        const uint32_t bytes = kABytes + nt * kStageK + kImgBytes + 16;
+        const bool shared_e = a.x == p.E;
+        const CUtensorMap* tma = shared_e ? &p.tm_a_shared : &p.tm_a;
+        const int row_base = shared_e ? 0 : a.x * p.a_rows;
+        const uint4* sfa = p.sfa + (static_cast<size_t>(a.x) * p.tiles + t) * G;
+        const uint8_t* sfb = p.sfb + static_cast<size_t>(u) * G * kImgBytes;
+        for (int g = 0; g < G; ++g, ++it) {
+          const int s = it % kStages;
+          const uint32_t round = it / kStages;
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty[s]), (round & 1) ^ 1, abort,
+                              kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = ptx::smem_u32(&bars->full[s]);
+          ptx::mbar_arrive_expect_tx(full, bytes);
+          const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
+          const int x = g * kStageK;
+          if (PHASE == 13) {
+            ptx::tma_load_2d(sa, tma, x, row_base + 64 * t, full, pol_w);
+            ptx::tma_load_2d(sa + kABytes / 2, tma, x, row_base + p.inter + 64 * t, full, pol_w);
+          } else {
+            ptx::tma_load_2d(sa, tma, x, row_base + kTileM * t, full, pol_w);
+          }
+          const uint32_t sb = ptx::smem_u32(smem + kOffB + s * kBBytes);
+          for (int b = 0; b < nt / kBoxRows; ++b)
+            ptx::tma_load_2d(sb + b * kBoxRows * kStageK, &p.tm_b, x, a.y + b * kBoxRows, full,
+                             pol_x);
+          ptx::bulk_load(ptx::smem_u32(smem + kOffSfb + s * kImgBytes), sfb + g * kImgBytes,
+                         kImgBytes, full);
+          ptx::bulk_load(ptx::smem_u32(smem + kOffSfac + s * 16), sfa + g, 16, full);
+        }
+      }
+      // wait for every copy still in flight before the CTA may exit
+      const uint32_t issued = it;
+      for (int s = 0; s < kStages; ++s) {
+        if (static_cast<uint32_t>(s) < issued) {
+          const uint32_t last_round = (issued - 1 - s) / kStages;
+          drain_wait(ptx::smem_u32(&bars->full[s]), last_round & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t it = 0;
+    int lt = 0;
+    bool ok = true;
+    for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
+      const int u = task / p.tiles;
+      const int4 a = act[u];
+      if (!task_valid(a, p)) continue;
+      const int nt = (a.z + 15) & ~15;
+      const int acc = lt & 1;
+      const uint32_t use = static_cast<uint32_t>(lt) >> 1;
+      ++lt;
+      if (!warp_wait(ptx::smem_u32(&bars->tempty[acc]), (use & 1) ^ 1, abort)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tbase + acc * kAccCols;
+      for (int g = 0; g < G; ++g, ++it) {
+        const int s = it % kStages;
+        const uint32_t round = it / kStages;
+        if (!warp_wait(ptx::smem_u32(&bars->full[s]), round & 1, abort)) {
+          ok = false;
+          break;
+        }
+        // the stage's weight-scale entry -> 32 identical 16-byte image rows
+        const uint4 cmp = *reinterpret_cast<const uint4*>(smem + kOffSfac + s * 16);
+        *reinterpret_cast<uint4*>(smem + kOffSfa + s * kImgBytes + lane * 16) = cmp;
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tc_fence_after();
+          const uint32_t sf_a = tbase + kSfCol0 + s * 8;
+          const uint32_t sf_b = sf_a + 4;
+          ptx::tc_cp_32x128b_x4(sf_a, ptx::sdesc_rows16(ptx::smem_u32(smem + kOffSfa + s * kImgBytes)));
+          ptx::tc_cp_32x128b_x4(sf_b, ptx::sdesc_rows16(ptx::smem_u32(smem + kOffSfb + s * kImgBytes)));
+          const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
+          const uint32_t sb = ptx::smem_u32(smem + kOffB + s * kBBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            ptx::tc_mma_mxf8(d_tmem, ptx::sdesc_k128_sw128(sa + 32 * k),
+                             ptx::sdesc_k128_sw128(sb + 32 * k), ptx::idesc_mxf8_e4m3(nt, k), sf_a,
+                             sf_b, (g | k) != 0);
+          }
+          ptx::tc_commit(ptx::smem_u32(&bars->empty[s]));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::tc_commit(ptx::smem_u32(&bars->tfull[acc]));
+      __syncwarp();
+    }
+    // every MMA / copy this thread issued has completed once drain fires
+    if (lane == 0) {
+      ptx::tc_commit(ptx::smem_u32(&bars->drain));
+      drain_wait(ptx::smem_u32(&bars->drain), 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp - 4;  // TMEM lane quarter
+    float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [n][64] up values
+    int lt = 0;
+    for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
+      const int u = task / p.tiles, t = task - u * p.tiles;
+      const int4 a = act[u];
+      if (!task_valid(a, p)) continue;
+      const int rows = a.z;
+      const int nt = (rows + 15) & ~15;
+      const int acc = lt & 1;
+      const uint32_t use = static_cast<uint32_t>(lt) >> 1;
+      ++lt;
+      const uint32_t tfull = ptx::smem_u32(&bars->tfull[acc]);
+      if (threadIdx.x == 128) misc->epi_ok = ptx::mbar_wait(tfull, use & 1, abort, kWaitLimitNs);
+      epi_bar();
+      if (!*reinterpret_cast<volatile int*>(&misc->epi_ok)) break;
+      ptx::mbar_wait(tfull, use & 1, abort, kWaitLimitNs);  // completed: returns at once
+      ptx::tc_fence_after();
+      float v[kMaxTokens];
+      const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * q) << 16) + acc * kAccCols;
+      ptx::tmem_ld_32x32b_x16(taddr, v);
+      if (nt > 16) ptx::tmem_ld_32x32b_x16(taddr + 16, v + 16);
+      if (nt > 32) ptx::tmem_ld_32x32b_x16(taddr + 32, v + 32);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->tempty[acc]));
+
+      if (PHASE == 2) {
+        float* dst = p.part + static_cast<size_t>(a.y) * p.hidden + kTileM * t + 32 * q + lane;
+#pragma unroll
+        for (int n = 0; n < kMaxTokens; ++n)
+          if (n < rows) dst[static_cast<size_t>(n) * p.hidden] = v[n];
+      } else {
+        if (q >= 2) {
+#pragma unroll
+          for (int n = 0; n < kMaxTokens; ++n)
+            if (n < rows) xchg[n * 64 + 32 * (q - 2) + lane] = v[n];
+        }
+        epi_bar();
+        if (q < 2) {
+          const int i = 64 * t + 32 * q + lane;  // intermediate column
+          const int kb = i >> 5;                 // its 32-column block
+          uint8_t* hrow = p.h8 + static_cast<size_t>(a.y) * p.inter + i;
+          uint8_t* img = p.sfb_next + (static_cast<size_t>(u) * p.next_G + (kb >> 2)) * kImgBytes +
+                         (kb & 3);
+#pragma unroll
+          for (int n = 0; n < kMaxTokens; ++n) {
+            if (n < rows) {
+              const float gv = v[n];
+              const float uv = xchg[n * 64 + 32 * q + lane];
+              const float h = (gv / (1.0f + expf(-gv))) * uv;
+              float amax = fabsf(h);
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+              const int code = mx_code(amax);
+              hrow[static_cast<size_t>(n) * p.inter] = e4m3(clamp_e4m3(h * mx_mul(code)));
+              if (lane == 0) img[(n & 31) * 16 + (n >> 5) * 4] = static_cast<uint8_t>(code);
+            }
+          }
+        }
+      }
+      epi_bar();
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tbase, kTmemCols);
+  }
+  if (threadIdx.x == 0 && misc->abort) atomicOr(p.err, kErrTimeout);
+}
+
+}  // namespace
+
+size_t expert_smem_bytes(int) { return kSmemBytes; }
+
+cudaError_t expert_kernel_setup() {
+  cudaError_t e = cudaFuncSetAttribute(expert_kernel<13>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(expert_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemBytes));
+}
+
+cudaError_t launch_expert13(const ExpertParams& p, int grid, cudaStream_t s) {
+  expert_kernel<13><<<grid, kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expert2(const ExpertParams& p, int grid, cudaStream_t s) {
+  expert_kernel<2><<<grid, kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -104,14 +104,19 @@ def _bf16(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
 
 
+def token_row(wl: Workload, t: int, attempt: int = 0) -> torch.Tensor:
+    """Row t of x (bf16 [1, H], host), draw number ``attempt`` of that row."""
+    r = _rng(wl.seed, _TAG_X, t, attempt).standard_normal(wl.dims.hidden, dtype=np.float32)
+    return _bf16(r[None, :])
+
+
 def token_rows(wl: Workload, attempts=None, m: int | None = None) -> torch.Tensor:
     """x bf16 [m, H] on the host; row t drawn from stream (seed, t, attempts[t])."""
     m = wl.tokens if m is None else m
     attempts = [0] * m if attempts is None else list(attempts)
-    h = wl.dims.hidden
-    rows = [_rng(wl.seed, _TAG_X, t, attempts[t]).standard_normal(h, dtype=np.float32)
-            for t in range(m)]
-    return _bf16(np.stack(rows) if rows else np.zeros((0, h), np.float32))
+    if m == 0:
+        return torch.zeros(0, wl.dims.hidden, dtype=torch.bfloat16)
+    return torch.cat([token_row(wl, t, attempts[t]) for t in range(m)])
 
 
 def router_inputs(wl: Workload) -> dict:

@@ -1,0 +1,144 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bar (per workload): E4M3 bytes and E8M0 codes of the seam bit-exact (taken on
+the GPU's own normed row, since the fp32 norm may differ from the float64
+oracle by one bf16 ulp at a rounding boundary); normed within 1 bf16 ulp;
+top-k expert ids bit-exact as ordered lists (inputs drawn with every top-k gap
+> 1e-3); routing weights within 1e-5 relative; the bf16 output within a
+normwise relative error of 5e-3 of the oracle.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp8_moe_decode_gb300 import workloads as W
+from oracle import moe as O
+
+from _harness import Layer, bf16_ulp_diff, f64, gapped_tokens, rel_err
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 5e-3
+W_RTOL = 1e-5
+
+
+def check(L: Layer, x: torch.Tensor, tokens=None, label=""):
+    out, dbg = L.run(x)
+    ref = L.oracle(x, tokens=tokens)
+    m = x.shape[0]
+    # seam
+    ulp = bf16_ulp_diff(f64(dbg["normed"]), ref.normed)
+    assert ulp.max() <= 1, (label, int(ulp.max()))
+    xb, xc = O.seam_quant(f64(dbg["normed"]))
+    assert np.array_equal(dbg["x8"].numpy(), xb), label
+    assert np.array_equal(dbg["x8_codes"].numpy(), xc), label
+    same = ulp.reshape(m, -1, 32).max(-1) == 0  # groups whose normed values agree
+    assert np.array_equal(dbg["x8_codes"].numpy()[same], ref.codes[same]), label
+    # router
+    assert np.array_equal(dbg["topk_ids"].numpy(), ref.routing.ids), label
+    np.testing.assert_allclose(dbg["topk_w"].numpy(), ref.routing.weights, rtol=W_RTOL)
+    np.testing.assert_allclose(dbg["logits"].numpy(), ref.routing.logits, rtol=1e-3, atol=1e-4)
+    # output
+    rows = list(range(m)) if tokens is None else list(tokens)
+    err = rel_err(f64(out)[rows], ref.out[rows])
+    assert err <= OUT_TOL, (label, err)
+    assert L.layer.status() == 0
+    return err, int((ulp > 0).sum())
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    L = Layer(W.WORKLOADS["tiny_m1"])
+    yield L
+    L.close()
+
+
+def test_tiny_m1(tiny):
+    x, _ = gapped_tokens(tiny.wl, tiny.ri)
+    err, nd = check(tiny, x, label="tiny_m1")
+    print(f"tiny_m1: rel err {err:.2e}, normed ulp diffs {nd}")
+
+
+@pytest.mark.parametrize("m", [2, 3, 7, 15, 16, 17, 31, 32, 33, 47, 48])
+def test_tiny_ragged_m(tiny, m):
+    # every MMA N (16 / 32 / 48) and ragged token counts per expert
+    x, _ = gapped_tokens(tiny.wl, tiny.ri, m=m)
+    err, _ = check(tiny, x, label=f"tiny m={m}")
+    assert err <= OUT_TOL
+
+
+def test_tiny_special_rows(tiny):
+    # an all-zero row (codes 0, bytes 0) and tiny negatives next to large values
+    # (bytes 0x80); the zero row's routing is decided by the bias alone
+    x, _ = gapped_tokens(tiny.wl, tiny.ri, m=4)
+    x[1] = 0
+    x[2, ::7] = -1e-30
+    out, dbg = tiny.run(x)
+    ref = tiny.oracle(x)
+    xb, xc = O.seam_quant(f64(dbg["normed"]))
+    assert np.array_equal(dbg["x8"].numpy(), xb) and np.array_equal(dbg["x8_codes"].numpy(), xc)
+    assert np.all(dbg["x8"].numpy()[1] == 0) and np.all(dbg["x8_codes"].numpy()[1] == 0)
+    assert np.any(dbg["x8"].numpy()[2] == 0x80)
+    assert np.array_equal(dbg["topk_ids"].numpy(), ref.routing.ids)
+    rows = [0, 2, 3]
+    assert rel_err(f64(out)[rows], ref.out[rows]) <= OUT_TOL
+    assert np.all(np.isfinite(f64(out)))
+
+
+def test_tiny_deterministic_and_graph(tiny):
+    x, _ = gapped_tokens(tiny.wl, tiny.ri, m=5)
+    xd = x.to(tiny.dev)
+    a = tiny.layer.step(xd).clone()
+    b = tiny.layer.step(xd).clone()
+    assert torch.equal(a, b)
+    s = torch.cuda.Stream(tiny.dev)
+    out = torch.empty_like(xd)
+    s.wait_stream(torch.cuda.current_stream(tiny.dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        tiny.layer.step(xd, out=out)  # warm-up on the capture stream
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            tiny.layer.step(xd, out=out, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, a)
+    assert tiny.layer.status() == 0
+
+
+def test_tiny_range_errors(tiny):
+    from mxfp8_moe_decode_gb300._lib import MOE_ERR_RANGE, MoeError
+    d = tiny.wl.dims
+    for m in (0, d.max_tokens + 1):
+        x = torch.zeros(m, d.hidden, dtype=torch.bfloat16, device=tiny.dev)
+        with pytest.raises(MoeError) as ei:
+            tiny.layer.step(x)
+        assert ei.value.code == MOE_ERR_RANGE
+
+
+def test_small_m4():
+    L = Layer(W.WORKLOADS["small_m4"])
+    try:
+        x, _ = gapped_tokens(L.wl, L.ri)
+        err, nd = check(L, x, label="small_m4")
+        print(f"small_m4: rel err {err:.2e}, normed ulp diffs {nd}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("name,sample", [("full_m1", None), ("full_m16", [0, 7, 15]),
+                                         ("full_m48_uniform", [0, 23, 47]),
+                                         ("full_m48_zipf", [0, 23, 47])])
+def test_full_size(name, sample):
+    L = Layer(W.WORKLOADS[name])
+    try:
+        x, _ = gapped_tokens(L.wl, L.ri)
+        err, nd = check(L, x, tokens=sample, label=name)
+        print(f"{name}: rel err {err:.2e} on tokens {sample}, normed ulp diffs {nd}, "
+              f"unique routed experts {L.layer.unique_experts()}")
+    finally:
+        L.close()
+        del L
+        torch.cuda.empty_cache()
