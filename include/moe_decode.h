@@ -172,7 +172,9 @@ int moe_last_unique_experts(moe_handle* h, int* unique_routed);
  * Timing hooks for profiling: while set, every step records events[i]
  * (cudaEvent_t values, caller-owned) on its stream just before kernel i and
  * events[n_kernels] after the last kernel; n must equal moe_kernel_count()+1.
- * Pass events = NULL, n = 0 to turn it off.
+ * Pass events = NULL, n = 0 to turn it off. Inside a stream capture the
+ * records become event-record nodes of the graph: the events must then outlive
+ * every graph (and graph exec) captured with them.
  */
 int moe_set_timing_events(moe_handle* h, void* const* events, int n);
 

@@ -350,8 +350,16 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   const int H = h->cfg.hidden, E = h->cfg.experts, K = h->cfg.topk;
   const bool timed = h->n_events == kNumKernels + 1;
   cudaError_t err = cudaSuccess;
+  // under stream capture a plain record only adds a dependency; an external
+  // record becomes an event-record node that fires at every graph replay
+  unsigned int rec_flags = cudaEventRecordDefault;
+  if (timed) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    err = cudaStreamIsCapturing(st, &cs);
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+  }
   auto mark = [&](int i) {
-    if (timed && err == cudaSuccess) err = cudaEventRecord(h->events[i], st);
+    if (timed && err == cudaSuccess) err = cudaEventRecordWithFlags(h->events[i], st, rec_flags);
   };
 
   SeamParams sp;
