@@ -210,6 +210,47 @@ const char* moe_strerror(int code);
 /* Frees the handle's scratch and the handle (NULL is allowed). */
 void moe_destroy(moe_handle* h);
 
+/*
+ * Allocation-free routing. The source pages have no counterpart to this entry
+ * point; it is an addition of this library for callers that may not allocate
+ * device memory when they route: an engine whose memory is all handed out by
+ * its own pool (or planned before it starts) cannot have a library call
+ * cudaMalloc behind its back, code running inside a CUDA graph capture cannot
+ * call cudaMalloc at all, and a caller that only needs routing decisions for
+ * rows it already normalised should not need a moe_create handle (which
+ * allocates the whole step's scratch).
+ *
+ * Computes, for M bf16 rows `normed` [M, hidden] (device), the router of
+ * moe_decode_step: logits against gate_w bf16 [experts, hidden] (device),
+ * scores sigmoid(logit), the topk experts of score + bias (bias f32
+ * [experts], device; ties to the lower index) in decreasing order into
+ * topk_ids i32 [M, topk] (device), and their scores over the chosen scores'
+ * sum into topk_w f32 [M, topk] (device). The caller owns every buffer;
+ * nothing is allocated: the kernel's scratch is one fixed device array of
+ * MOE_ROUTE_STATIC_SCRATCH_BYTES inside the library, held by every GPU that
+ * loads the library until the process exits.
+ *
+ * Limits: 1 <= M <= 48; hidden a multiple of 128 in [256, 8192]; experts a
+ * multiple of 32 in [32, 512]; 1 <= topk <= 16. A problem whose scratch
+ * (logit partials, about 4 * 1024 * M bytes, plus small routing tables) would
+ * not fit the array is refused with MOE_ERR_UNSUPPORTED before anything is
+ * enqueued (e.g. experts = 512 with hidden > 4096). Other errors:
+ * MOE_ERR_ARG (null pointer), MOE_ERR_ALIGN (normed / gate_w not 16-byte
+ * aligned, the others not 4-byte aligned), MOE_ERR_RANGE (M), MOE_ERR_CUDA.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address and sets the kernel's shared-memory limit; make that first
+ * call before any stream capture. Each call enqueues a memset of the array's
+ * counters and one kernel on `stream` (void* holding a cudaStream_t). All
+ * calls share the one array, which keeps the last call's contents: calls whose
+ * work overlaps on the GPU (different streams, or concurrent host threads
+ * without ordering) race on it and must be serialised by the caller.
+ */
+#define MOE_ROUTE_STATIC_SCRATCH_BYTES (256 * 1024)
+int moe_route_static(const void* normed, const void* gate_w, const float* bias, int M,
+                     int hidden, int experts, int topk, int32_t* topk_ids, float* topk_w,
+                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,136 @@
+// Allocation-free routing entry point: the router kernel (gate GEMV, sigmoid,
+// bias-adjusted top-k, normalised weights) run with its scratch in a fixed
+// file-scope device array instead of memory the library allocates.
+//
+// Who needs this: callers that may not allocate device memory at the time
+// they route. A serving engine that hands all GPU memory to its own pool, or
+// that plans every buffer before it starts, cannot let a library call
+// cudaMalloc behind its back; code that runs while a CUDA graph is being
+// captured cannot call cudaMalloc at all (the call is illegal there and breaks
+// the capture); and a caller that only wants routing decisions for rows it has
+// already normalised does not want a whole moe_create handle, which allocates
+// the full step's scratch. Here the caller passes its inputs and outputs and
+// nothing is allocated.
+//
+// The array is a static __device__ object of kStaticScratchBytes: every GPU
+// that loads the library holds it until the process exits. Host code may not
+// use the array's name as a device address (on the host it names a stand-in
+// object), so the device address is looked up once per device with
+// cudaGetSymbolAddress and handed to the kernel.
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = 256 * 1024;
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) uint8_t g_route_scratch[kStaticScratchBytes];
+
+std::mutex g_mu;
+void* g_addr[kMaxDevices];
+bool g_ready[kMaxDevices];
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// First call on a device (that device current): find the array's device
+// address and raise the router kernel's shared-memory limit.
+int device_scratch(int dev, void** addr) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  if (!g_ready[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    e = moe::router_setup();
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    g_addr[dev] = p;
+    g_ready[dev] = true;
+  }
+  *addr = g_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_route_static(const void* normed, const void* gate_w, const float* bias, int M,
+                                int hidden, int experts, int topk, int32_t* topk_ids,
+                                float* topk_w, void* stream) {
+  using namespace moe;
+  if (!normed || !gate_w || !bias || !topk_ids || !topk_w) return MOE_ERR_ARG;
+  if (!aligned(normed, 16) || !aligned(gate_w, 16) || !aligned(bias, 4) ||
+      !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+    return MOE_ERR_ALIGN;
+  if (M < 1 || M > kMaxTokens) return MOE_ERR_RANGE;
+  if (hidden % 128 || hidden < 256 || hidden > 8192) return MOE_ERR_UNSUPPORTED;
+  if (experts % 32 || experts < 32 || experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (topk < 1 || topk > kMaxTopk || topk > experts) return MOE_ERR_UNSUPPORTED;
+
+  // the router's K-split: about 128 CTAs, slices <= 2048 columns
+  int ks = 128 / (experts / kRouterWarps);
+  if (ks < 1) ks = 1;
+  if (ks > 16) ks = 16;
+  while (hidden / ks > 2048) ks *= 2;
+  while (hidden % (ks * 8)) ks /= 2;
+
+  // layout inside the static array; refuse problems that do not fit
+  const size_t o_ctr = 0;
+  const size_t o_act = o_ctr + align256(kCtrWords * 4);
+  const size_t o_rw = o_act + align256(static_cast<size_t>(experts + 1) * sizeof(ActiveExpert));
+  const size_t o_tp = o_rw + align256(static_cast<size_t>(M) * topk * 4);
+  const size_t o_pt = o_tp + align256(static_cast<size_t>(M) * (topk + 1) * 4);
+  const size_t o_lp = o_pt + align256(static_cast<size_t>(M) * (topk + 1) * 4);
+  const size_t need = o_lp + align256(static_cast<size_t>(ks) * M * experts * 4);
+  if (need > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  void* base_v = nullptr;
+  const int rc = device_scratch(dev, &base_v);
+  if (rc != MOE_OK) return rc;
+  uint8_t* base = static_cast<uint8_t*>(base_v);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // the router's completion ticket (and error word) must start at zero; the
+  // array keeps whatever the previous call left
+  if (cudaMemsetAsync(base + o_ctr, 0, kCtrWords * 4, st) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  RouterParams rp;
+  rp.normed = static_cast<const __nv_bfloat16*>(normed);
+  rp.gate_w = static_cast<const __nv_bfloat16*>(gate_w);
+  rp.bias = bias;
+  rp.logit_part = reinterpret_cast<float*>(base + o_lp);
+  rp.counters = reinterpret_cast<int*>(base + o_ctr);
+  rp.act = reinterpret_cast<ActiveExpert*>(base + o_act);
+  rp.route_w = reinterpret_cast<float*>(base + o_rw);
+  rp.tok_pos = reinterpret_cast<int*>(base + o_tp);
+  rp.pos_tok = reinterpret_cast<int*>(base + o_pt);
+  rp.dbg_ids = topk_ids;
+  rp.dbg_w = topk_w;
+  rp.dbg_logits = nullptr;
+  rp.M = M;
+  rp.H = hidden;
+  rp.E = experts;
+  rp.K = topk;
+  rp.KS = ks;
+  rp.Hs = hidden / ks;
+  if (launch_router(rp, st) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
