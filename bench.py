@@ -44,6 +44,7 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-experts", type=int, default=4,
                     help="experts the CPU baseline evaluates per sample")
     return ap.parse_args()
@@ -160,65 +161,13 @@ def make_layer(wl, dev, ew=None):
     return layer, x, ew
 
 
-def time_layer(layer, x, dev, steps: int, warmup: int, flush, with_kernel_events=True):
-    """Graph-replay timing: per step flush L2 (untimed), then events around the
-    replay. Returns (per-step ms list, per-kernel mean ms list, unique routed).
-    The graph is released before its timing events."""
-    import torch
-
-    from mxfp8_moe_decode_gb300 import kernel_names
-
-    nk = len(kernel_names())
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-    if with_kernel_events:
-        layer.set_timing_events(evs)
-    out = torch.empty_like(x)
-    s = torch.cuda.Stream(dev)
-    s.wait_stream(torch.cuda.current_stream(dev))
-    with torch.cuda.stream(s):
-        for _ in range(max(warmup, 3)):
-            layer.step(x, out=out, stream=s)
-        torch.cuda.synchronize(dev)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            layer.step(x, out=out, stream=s)
-    torch.cuda.synchronize(dev)
-    if layer.status() != 0:
-        raise RuntimeError(f"device status {layer.status()}")
-    unique = layer.unique_experts()
-    for _ in range(warmup):
-        flush()
-        g.replay()
-    torch.cuda.synchronize(dev)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms, kern = [], [[] for _ in range(nk)]
-    cur = torch.cuda.current_stream(dev)
-    for _ in range(steps):
-        flush()
-        t0.record(cur)
-        g.replay()
-        t1.record(cur)
-        t1.synchronize()
-        step_ms.append(t0.elapsed_time(t1))
-        if with_kernel_events:
-            for i in range(nk):
-                kern[i].append(evs[i].elapsed_time(evs[i + 1]))
-    torch.cuda.synchronize(dev)
-    layer.set_timing_events(None)
-    if layer.status() != 0:
-        raise RuntimeError(f"device status {layer.status()}")
-    kmean = [statistics.mean(k) if k else None for k in kern]
-    # the graph holds record nodes of `evs`: drop it before the events go away
-    del g
-    torch.cuda.synchronize(dev)
-    return step_ms, kmean, unique
-
-
-def capture_plain(layer, x, dev):
-    """A graph of one step without timing events (for the end-to-end leg)."""
+def capture(layer, x, dev, events=None):
+    """A CUDA graph of one step (per-kernel timing events recorded as graph
+    nodes when `events` is given; the events must outlive the graph)."""
     import torch
 
     out = torch.empty_like(x)
+    layer.set_timing_events(events)
     s = torch.cuda.Stream(dev)
     s.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(s):
@@ -228,7 +177,60 @@ def capture_plain(layer, x, dev):
         with torch.cuda.graph(g, stream=s):
             layer.step(x, out=out, stream=s)
     torch.cuda.synchronize(dev)
+    layer.set_timing_events(None)
     return g, out
+
+
+def time_layer(layer, x, dev, steps: int, warmup: int, flush):
+    """Graph-replay timing. The step time comes from a graph without timing
+    events (kernels overlap through programmatic dependent launch); the
+    per-kernel breakdown from a second graph with an event node between
+    kernels. L2 is flushed (untimed) before every replay.
+    Returns (per-step ms, per-kernel mean ms, unique routed, graph, out)."""
+    import torch
+
+    from mxfp8_moe_decode_gb300 import kernel_names
+
+    for _ in range(max(warmup, 3)):
+        layer.step(x)
+    torch.cuda.synchronize(dev)
+    g, out = capture(layer, x, dev)
+    if layer.status() != 0:
+        raise RuntimeError(f"device status {layer.status()}")
+    unique = layer.unique_experts()
+    cur = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        flush()
+        g.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms = []
+    for _ in range(steps):
+        flush()
+        t0.record(cur)
+        g.replay()
+        t1.record(cur)
+        t1.synchronize()
+        step_ms.append(t0.elapsed_time(t1))
+
+    nk = len(kernel_names())
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    gk, _ = capture(layer, x, dev, events=evs)
+    kern = [[] for _ in range(nk)]
+    for i in range(warmup + steps):
+        flush()
+        gk.replay()
+        evs[-1].synchronize()
+        if i >= warmup:
+            for k in range(nk):
+                kern[k].append(evs[k].elapsed_time(evs[k + 1]))
+    torch.cuda.synchronize(dev)
+    del gk  # the graph holds record nodes of `evs`: drop it before the events
+    torch.cuda.synchronize(dev)
+    if layer.status() != 0:
+        raise RuntimeError(f"device status {layer.status()}")
+    kmean = [statistics.mean(k) for k in kern]
+    return step_ms, kmean, unique, g, out
 
 
 def run_gpu(args):
@@ -259,7 +261,8 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     with Clocks(local) as clk:
-        step_ms, kmean, unique = time_layer(layer, x, dev, args.steps, args.warmup, flush)
+        step_ms, kmean, unique, graph, out = time_layer(layer, x, dev, args.steps, args.warmup,
+                                                        flush)
     clocks = clk.summary()
     total_ms = sum(step_ms)
     if world > 1:
@@ -280,7 +283,6 @@ def run_gpu(args):
     step_gbs = alg / (us_step * 1e-6) / 1e9 if world == 1 else None
 
     # end to end: host (pinned) x -> device, the step, device out -> host
-    graph, out = capture_plain(layer, x, dev)
     xh = x.cpu().pin_memory()
     oh = torch.empty_like(xh).pin_memory()
     cur = torch.cuda.current_stream(dev)
@@ -316,7 +318,8 @@ def run_gpu(args):
                 prev_ew = None
                 torch.cuda.empty_cache()
             L2, x2, ew2 = make_layer(swl, dev, ew=reuse)
-            ms, km, u2 = time_layer(L2, x2, dev, max(5, args.steps // 2), 3, flush)
+            ms, km, u2, g2, _ = time_layer(L2, x2, dev, max(5, args.steps // 2), 3, flush)
+            del g2
             us2 = statistics.mean(ms) * 1e3
             a2 = W.algorithmic_bytes(swl.dims, u2)
             i2 = (u2 + 1) * (2 * swl.dims.inter * swl.dims.hidden
@@ -350,7 +353,8 @@ def run_gpu(args):
                    "alg_bytes_per_step": alg, "step_gbs": round(step_gbs, 1) if step_gbs else None,
                    "step_frac_of_peak": round(step_gbs / peaks["hbm_gbs"], 4) if step_gbs else None,
                    "l2": "flushed (512 MB write) before every timed step; weights > L2",
-                   "timing": "CUDA-graph replay, CUDA events per step",
+                   "timing": "CUDA-graph replay, CUDA events per step; kernel_us from a second graph "
+                  "with event nodes between kernels",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline,
         "kernel_us": {n: round(k * 1e3, 2) for n, k in zip(names, kmean)},
@@ -361,7 +365,7 @@ def run_gpu(args):
     }
     if sweep:
         line["sweep"] = sweep
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_experts, unique)
     if world > 1:
         dist.barrier()

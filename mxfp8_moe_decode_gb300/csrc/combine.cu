@@ -8,6 +8,7 @@
 //
 // Grid (ceil(H / 1024), M) x 128 threads; a thread owns 8 adjacent columns.
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -15,6 +16,8 @@ namespace {
 constexpr int kThreads = 128;
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
+  ptx::griddep_wait();  // partial rows come from the w2 kernel
+  ptx::griddep_launch_dependents();
   const int m = blockIdx.y;
   const int H = p.H, K = p.K;
   const int col = (blockIdx.x * kThreads + threadIdx.x) * 8;
@@ -60,8 +63,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   dim3 grid((p.H / 8 + kThreads - 1) / kThreads, p.M);
-  combine_kernel<<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(kThreads), 0, s, p);
 }
 
 }  // namespace moe

@@ -29,6 +29,11 @@
 // allocation; warps 4-7 drain the double-buffered accumulator (each reads its
 // 32-lane quarter). Every mbarrier wait is bounded; on a timeout the CTA
 // records kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
+//
+// Launched with programmatic dependent launch: the prologue (barriers, TMEM,
+// descriptor prefetch) and the first task's weight stages run while the
+// previous kernel finishes; the activation operands and every global write
+// wait for it (griddepcontrol.wait).
 #include "internal.cuh"
 #include "mx.cuh"
 #include "ptx.cuh"
@@ -132,8 +137,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tbase = misc->tmem_base;
+  // the next kernel may start launching: it waits for this grid before it
+  // reads anything this grid writes
+  ptx::griddep_launch_dependents();
 
-  int units = p.counters[kCtrUnits];
+  // The routing tables were written by the router, two kernels back: it has
+  // completed before this grid could launch (every kernel of the step waits
+  // for its predecessor before it lets the next one start). Read them past L1.
+  int units = __ldcg(p.counters + kCtrUnits);
   if (units < 0 || units > p.units_max) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
     units = 0;
@@ -149,9 +160,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
+      // The first task's weight tiles (and their scale entries) do not depend
+      // on the previous kernel: they are issued for the whole ring before the
+      // grid-dependency wait; the activation halves of those stages follow it.
+      bool waited = false;
+      int first_pending = 0, n_pending = 0;
       for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
         const int u = task / p.tiles, t = task - u * p.tiles;
-        const int4 a = act[u];
+        const int4 a = __ldcg(act + u);
         if (!task_valid(a, p)) continue;
         const int nt = (a.z + 15) & ~15;
         const uint32_t bytes = kABytes + nt * kStageK + kImgBytes + 16;
@@ -160,6 +176,15 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         const int row_base = shared_e ? 0 : a.x * p.a_rows;
         const uint4* sfa = p.sfa + (static_cast<size_t>(a.x) * p.tiles + t) * G;
         const uint8_t* sfb = p.sfb + static_cast<size_t>(u) * G * kImgBytes;
+        auto issue_b = [&](int g, int s) {
+          const uint32_t full = ptx::smem_u32(&bars->full[s]);
+          const uint32_t sb = ptx::smem_u32(smem + kOffB + s * kBBytes);
+          for (int b = 0; b < nt / kBoxRows; ++b)
+            ptx::tma_load_2d(sb + b * kBoxRows * kStageK, &p.tm_b, g * kStageK,
+                             a.y + b * kBoxRows, full, pol_x);
+          ptx::bulk_load(ptx::smem_u32(smem + kOffSfb + s * kImgBytes), sfb + g * kImgBytes,
+                         kImgBytes, full);
+        };
         for (int g = 0; g < G; ++g, ++it) {
           const int s = it % kStages;
           const uint32_t round = it / kStages;
@@ -178,15 +203,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           } else {
             ptx::tma_load_2d(sa, tma, x, row_base + kTileM * t, full, pol_w);
           }
-          const uint32_t sb = ptx::smem_u32(smem + kOffB + s * kBBytes);
-          for (int b = 0; b < nt / kBoxRows; ++b)
-            ptx::tma_load_2d(sb + b * kBoxRows * kStageK, &p.tm_b, x, a.y + b * kBoxRows, full,
-                             pol_x);
-          ptx::bulk_load(ptx::smem_u32(smem + kOffSfb + s * kImgBytes), sfb + g * kImgBytes,
-                         kImgBytes, full);
           ptx::bulk_load(ptx::smem_u32(smem + kOffSfac + s * 16), sfa + g, 16, full);
+          if (waited) {
+            issue_b(g, s);
+          } else {
+            if (n_pending == 0) first_pending = g;
+            ++n_pending;
+            if (n_pending == kStages || g == G - 1) {
+              ptx::griddep_wait();
+              waited = true;
+              for (int j = 0; j < n_pending; ++j) issue_b(first_pending + j, (first_pending + j) % kStages);
+              n_pending = 0;
+            }
+          }
         }
       }
+      if (!waited) ptx::griddep_wait();
       // wait for every copy still in flight before the CTA may exit
       const uint32_t issued = it;
       for (int s = 0; s < kStages; ++s) {
@@ -204,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     bool ok = true;
     for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
       const int u = task / p.tiles;
-      const int4 a = act[u];
+      const int4 a = __ldcg(act + u);
       if (!task_valid(a, p)) continue;
       const int nt = (a.z + 15) & ~15;
       const int acc = lt & 1;
@@ -260,10 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     // ------------------------------------------------------------ epilogue
     const int q = warp - 4;  // TMEM lane quarter
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [n][64] up values
+    ptx::griddep_wait();  // before writing rows the previous kernels may read
     int lt = 0;
     for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
       const int u = task / p.tiles, t = task - u * p.tiles;
-      const int4 a = act[u];
+      const int4 a = __ldcg(act + u);
       if (!task_valid(a, p)) continue;
       const int rows = a.z;
       const int nt = (rows + 15) & ~15;
@@ -348,13 +381,11 @@ cudaError_t expert_kernel_setup() {
 }
 
 cudaError_t launch_expert13(const ExpertParams& p, int grid, cudaStream_t s) {
-  expert_kernel<13><<<grid, kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(expert_kernel<13>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
 }
 
 cudaError_t launch_expert2(const ExpertParams& p, int grid, cudaStream_t s) {
-  expert_kernel<2><<<grid, kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(expert_kernel<2>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
 }
 
 }  // namespace moe

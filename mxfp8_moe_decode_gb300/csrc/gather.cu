@@ -17,6 +17,7 @@
 // c-th 32-row block for the stage's 4 K blocks. A w13 tile is 64 gate rows
 // (blocks 2t, 2t + 1) over the matching 64 up rows (blocks I/32 + 2t, + 1).
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -24,6 +25,8 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p) {
+  ptx::griddep_wait();  // routing tables and x8 come from the previous kernels
+  ptx::griddep_launch_dependents();
   const int H = p.H;
   const int rows = p.M * (p.K + 1);
   const int n16 = H >> 4;
@@ -102,8 +105,7 @@ __global__ void __launch_bounds__(kThreads) sfa_pack_kernel(const SfaPackParams 
 }  // namespace
 
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s) {
-  gather_kernel<<<2 * num_sms, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3(2 * num_sms), dim3(kThreads), 0, s, p);
 }
 
 cudaError_t launch_sfa_pack(const SfaPackParams& p, cudaStream_t s) {

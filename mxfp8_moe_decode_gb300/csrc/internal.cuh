@@ -131,6 +131,25 @@ struct SfaPackParams {
   int E, H, I;
 };
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream finishes; it must call griddep_wait()
+// before it reads that kernel's outputs or writes what that kernel reads.
+template <typename Kernel, typename Params>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_seam(const SeamParams& p, int M, cudaStream_t s);
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);

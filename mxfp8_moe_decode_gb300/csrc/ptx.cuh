@@ -26,6 +26,20 @@ __device__ __forceinline__ uint32_t elect_lane0() {
   return (threadIdx.x & 31) == 0;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// Block until every grid this one depends on (the previous kernel on the
+// stream, launched with programmatic serialisation) has completed and its
+// memory is visible. A no-op when the launch had no programmatic dependency.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel on the stream to start launching (it still blocks in
+// its own griddep_wait until this grid completes).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));

@@ -20,6 +20,7 @@
 #include <cmath>
 
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -47,16 +48,8 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = blockIdx.y * Hs;
 
-  // ---- stage the K-slice of the normed rows
-  uint4* xs = reinterpret_cast<uint4*>(smem);  // [M][Hs / 8]
-  const int oct = Hs >> 3;
-  for (int i = tid; i < M * oct; i += kThreads) {
-    const int m = i / oct, o = i - m * oct;
-    xs[i] = reinterpret_cast<const uint4*>(p.normed + static_cast<size_t>(m) * H + k0)[o];
-  }
-  __syncthreads();
-
-  // ---- one expert row per warp: lane holds 8 columns of every 256-chunk
+  // ---- one expert row per warp: lane holds 8 columns of every 256-chunk.
+  // The gate weights do not depend on the previous kernel: load them first.
   const int e = blockIdx.x * kRouterWarps + warp;
   uint4 g[kMaxChunks];
 #pragma unroll
@@ -68,6 +61,18 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
       g[c] = make_uint4(0, 0, 0, 0);
     }
   }
+  ptx::griddep_wait();  // the normed rows come from the seam kernel
+  ptx::griddep_launch_dependents();
+
+  // ---- stage the K-slice of the normed rows
+  uint4* xs = reinterpret_cast<uint4*>(smem);  // [M][Hs / 8]
+  const int oct = Hs >> 3;
+  for (int i = tid; i < M * oct; i += kThreads) {
+    const int m = i / oct, o = i - m * oct;
+    xs[i] = reinterpret_cast<const uint4*>(p.normed + static_cast<size_t>(m) * H + k0)[o];
+  }
+  __syncthreads();
+
   for (int m = 0; m < M; ++m) {
     float acc = 0.0f;
 #pragma unroll
@@ -98,7 +103,29 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
   for (int i = tid; i < E; i += kThreads) mask_s[i] = 0ull;
   __syncthreads();
 
+  // every logit of the step into shared memory (the K-slice staging is dead):
+  // the KS partials summed in a fixed order, all loads in flight at once
   const int KS = gridDim.y;
+  float* lg = reinterpret_cast<float*>(smem);  // [M][E]
+  {
+    const int n4 = M * E / 4;
+    const float4* lp = reinterpret_cast<const float4*>(p.logit_part);
+#pragma unroll 4
+    for (int i = tid; i < n4; i += kThreads) {
+      float4 a = __ldcg(lp + i);
+      for (int ks = 1; ks < KS; ++ks) {
+        const float4 b = __ldcg(lp + static_cast<size_t>(ks) * n4 + i);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      reinterpret_cast<float4*>(lg)[i] = a;
+      if (p.dbg_logits) reinterpret_cast<float4*>(p.dbg_logits)[i] = a;
+    }
+  }
+  __syncthreads();
+
   for (int m = warp; m < M; m += kRouterWarps) {
     float cv[kMaxPerLane], sv[kMaxPerLane];
 #pragma unroll
@@ -107,13 +134,10 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
       cv[i] = -INFINITY;
       sv[i] = 0.0f;
       if (ex < E) {
-        float logit = 0.0f;
-        for (int ks = 0; ks < KS; ++ks)
-          logit += __ldcg(&p.logit_part[(static_cast<size_t>(ks) * M + m) * E + ex]);
+        const float logit = lg[m * E + ex];
         const float s = 1.0f / (1.0f + expf(-logit));
         sv[i] = s;
         cv[i] = s + p.bias[ex];
-        if (p.dbg_logits) p.dbg_logits[static_cast<size_t>(m) * E + ex] = logit;
       }
     }
     float ssum = 0.0f;
@@ -238,20 +262,20 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
 }  // namespace
 
 size_t router_smem_bytes(int M, int Hs, int E) {
-  (void)E;
-  return static_cast<size_t>(M) * Hs * 2;
+  const size_t stage = static_cast<size_t>(M) * Hs * 2;  // normed K-slice
+  const size_t logits = static_cast<size_t>(M) * E * 4;  // the tail's logits
+  return stage > logits ? stage : logits;
 }
 
 cudaError_t router_setup() {
   return cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(router_smem_bytes(kMaxTokens, 2048, 0)));
+                              static_cast<int>(router_smem_bytes(kMaxTokens, 2048, kMaxExperts)));
 }
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
   const size_t smem = router_smem_bytes(p.M, p.Hs, p.E);
   dim3 grid(p.E / kRouterWarps, p.KS);
-  router_kernel<<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(router_kernel, grid, dim3(kThreads), smem, s, p);
 }
 
 }  // namespace moe

@@ -12,6 +12,7 @@
 // i, i + 128, ... so the 4 octets of a 32-group sit in 4 adjacent lanes.
 #include "internal.cuh"
 #include "mx.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -36,6 +37,9 @@ __global__ void __launch_bounds__(kThreads) seam_kernel(const SeamParams p) {
   const int tid = threadIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
   const uint4* wr = reinterpret_cast<const uint4*>(p.norm_w);
+  // x comes from the previous kernel on the stream; the router may start now
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   float v[kMaxOct][8];
   float ss = 0.0f;
@@ -110,8 +114,7 @@ __global__ void __launch_bounds__(kThreads) seam_kernel(const SeamParams p) {
 }  // namespace
 
 cudaError_t launch_seam(const SeamParams& p, int M, cudaStream_t s) {
-  seam_kernel<<<M, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(seam_kernel, dim3(M), dim3(kThreads), 0, s, p);
 }
 
 }  // namespace moe
