@@ -97,6 +97,21 @@ bool encode_rows(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3D uint8 tensor [planes][rows][cols] (strides cols and rows * cols bytes),
+// box = 128 bytes x box_rows x box_planes, 128-byte swizzle.
+bool encode_planes(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
+                   uint64_t planes, uint32_t box_rows, uint32_t box_planes) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cols, rows, planes};
+  const cuuint64_t strides[2] = {cols, rows * cols};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageK), box_rows, box_planes};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int validate_config(const moe_config* c) {
   if (c->hidden <= 0 || c->experts <= 0 || c->topk <= 0 || c->inter <= 0 ||
       c->shared_inter <= 0 || c->max_tokens <= 0 || !(c->eps >= 0.0f))
@@ -104,7 +119,7 @@ int validate_config(const moe_config* c) {
   if (c->hidden % 128 || c->hidden < 256 || c->hidden > 8192) return MOE_ERR_UNSUPPORTED;
   if (c->experts % 32 || c->experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (c->topk > kMaxTopk || c->topk > c->experts) return MOE_ERR_UNSUPPORTED;
-  if (c->inter % 128 || c->shared_inter != c->inter) return MOE_ERR_UNSUPPORTED;
+  if (c->inter % 128 || c->inter > 8192 || c->shared_inter != c->inter) return MOE_ERR_UNSUPPORTED;
   if (c->max_tokens > kMaxTokens) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -321,12 +336,16 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->p2.G = g2;
   h->p2.a_rows = H;
   h->p2.next_G = 0;
-  bool ok = encode_rows(&h->p13.tm_a, w->w13, H, static_cast<uint64_t>(E) * 2 * I, 64) &&
-            encode_rows(&h->p13.tm_a_shared, w->sw13, H, 2ull * I, 64) &&
-            encode_rows(&h->p13.tm_b, h->xg, H, h->rows_alloc, kBoxRows) &&
+  // w13 as [2E halves][I rows][H]: one box = 64 gate rows over the 64 matching up rows
+  bool ok = encode_planes(&h->p13.tm_a, w->w13, H, I, 2ull * E, 64, 2) &&
+            encode_planes(&h->p13.tm_a_shared, w->sw13, H, I, 2, 64, 2) &&
             encode_rows(&h->p2.tm_a, w->w2, I, static_cast<uint64_t>(E) * H, kTileM) &&
-            encode_rows(&h->p2.tm_a_shared, w->sw2, I, static_cast<uint64_t>(H), kTileM) &&
-            encode_rows(&h->p2.tm_b, h->h8, I, h->rows_alloc, kBoxRows);
+            encode_rows(&h->p2.tm_a_shared, w->sw2, I, static_cast<uint64_t>(H), kTileM);
+  for (int b = 0; b < 3 && ok; ++b) {
+    const uint32_t rows = static_cast<uint32_t>(kBoxRows * (b + 1));
+    ok = encode_rows(&h->p13.tm_b[b], h->xg, H, h->rows_alloc, rows) &&
+         encode_rows(&h->p2.tm_b[b], h->h8, I, h->rows_alloc, rows);
+  }
   if (!ok) {
     cudaFree(h->scratch);
     delete h;

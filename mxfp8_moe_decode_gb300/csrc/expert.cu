@@ -21,13 +21,17 @@
 //            h8 rows, K = I. Epilogue: fp32 rows of y for the combine.
 //
 // Per CTA (one per SM, 256 threads): warp 0 lane 0 issues the TMA loads into
-// an 8-stage ring (weights evict-first from L2; activations, scale entries and
-// scale images by TMA / bulk copies); warp 1 expands each stage's 16-byte
-// weight-scale entry into the 32 x 16-byte image tcgen05.cp expects, copies
-// both scale images into TMEM and issues 4 MMAs (K = 32 each, the descriptor's
-// scale-factor id picks the K block of the stage); warp 2 owns the TMEM
-// allocation; warps 4-7 drain the double-buffered accumulator (each reads its
-// 32-lane quarter). Every mbarrier wait is bounded; on a timeout the CTA
+// an 8-stage ring -- per stage one weight box (a w13 stage is one 3D box: the
+// 64 gate rows over the 64 matching up rows), one activation box (16 / 32 / 48
+// rows) and one bulk copy of the activation-scale image; weights evict-first
+// from L2. Warp 3 writes each stage's weight-scale image (the 16-byte entry of
+// the stage in all 32 rows tcgen05.cp expects) as soon as the slot is free.
+// Warp 1 lane 0 copies both scale images into TMEM and issues 4 MMAs (K = 32
+// each, the descriptor's scale-factor id picks the K block of the stage);
+// warp 2 owns the TMEM allocation; warps 4-7 drain the double-buffered
+// accumulator (each reads its 32-lane quarter). Every per-stage action is a
+// handful of single-thread instructions: at ~80 cycles per TMA or tcgen05
+// instruction, the issue cost per 16 KB stage sets the per-SM bandwidth. Every mbarrier wait is bounded; on a timeout the CTA
 // records kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
 //
 // Launched with programmatic dependent launch: the prologue (barriers, TMEM,
@@ -49,8 +53,7 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kImgBytes;
-constexpr uint32_t kOffSfac = kOffSfb + kStages * kImgBytes;
-constexpr uint32_t kOffXchg = kOffSfac + kStages * 16;
+constexpr uint32_t kOffXchg = kOffSfb + kStages * kImgBytes;
 constexpr uint32_t kOffBar = kOffXchg + kMaxTokens * 64 * 4;
 constexpr uint32_t kOffMisc = kOffBar + 256;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
@@ -65,8 +68,9 @@ static_assert(kSfCol0 + kStages * 8 <= kTmemCols, "TMEM budget");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kStages];     // weights + activations + activation scales landed
+  uint64_t empty[kStages];    // the stage's MMAs (and scale copies) completed
+  uint64_t sfa_rdy[kStages];  // the stage's weight-scale image is written
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -116,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->sfa_rdy[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_u32(&bars->tfull[a]), 1);
@@ -127,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&p.tm_a);
     ptx::prefetch_tmap(&p.tm_a_shared);
-    ptx::prefetch_tmap(&p.tm_b);
+    for (int b = 0; b < 3; ++b) ptx::prefetch_tmap(&p.tm_b[b]);
   }
   if (warp == 2) {
     ptx::tmem_alloc(ptx::smem_u32(&misc->tmem_base), kTmemCols);
@@ -170,18 +175,15 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         const int4 a = __ldcg(act + u);
         if (!task_valid(a, p)) continue;
         const int nt = (a.z + 15) & ~15;
-        const uint32_t bytes = kABytes + nt * kStageK + kImgBytes + 16;
+        const uint32_t bytes = kABytes + nt * kStageK + kImgBytes;
         const bool shared_e = a.x == p.E;
         const CUtensorMap* tma = shared_e ? &p.tm_a_shared : &p.tm_a;
-        const int row_base = shared_e ? 0 : a.x * p.a_rows;
-        const uint4* sfa = p.sfa + (static_cast<size_t>(a.x) * p.tiles + t) * G;
+        const CUtensorMap* tmb = &p.tm_b[nt / kBoxRows - 1];
         const uint8_t* sfb = p.sfb + static_cast<size_t>(u) * G * kImgBytes;
         auto issue_b = [&](int g, int s) {
           const uint32_t full = ptx::smem_u32(&bars->full[s]);
-          const uint32_t sb = ptx::smem_u32(smem + kOffB + s * kBBytes);
-          for (int b = 0; b < nt / kBoxRows; ++b)
-            ptx::tma_load_2d(sb + b * kBoxRows * kStageK, &p.tm_b, g * kStageK,
-                             a.y + b * kBoxRows, full, pol_x);
+          ptx::tma_load_2d(ptx::smem_u32(smem + kOffB + s * kBBytes), tmb, g * kStageK, a.y, full,
+                           pol_x);
           ptx::bulk_load(ptx::smem_u32(smem + kOffSfb + s * kImgBytes), sfb + g * kImgBytes,
                          kImgBytes, full);
         };
@@ -198,12 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
           const int x = g * kStageK;
           if (PHASE == 13) {
-            ptx::tma_load_2d(sa, tma, x, row_base + 64 * t, full, pol_w);
-            ptx::tma_load_2d(sa + kABytes / 2, tma, x, row_base + p.inter + 64 * t, full, pol_w);
+            // one box: the 64 gate rows (half 2e) over the matching 64 up rows (half 2e + 1)
+            ptx::tma_load_3d(sa, tma, x, 64 * t, shared_e ? 0 : 2 * a.x, full, pol_w);
           } else {
-            ptx::tma_load_2d(sa, tma, x, row_base + kTileM * t, full, pol_w);
+            ptx::tma_load_2d(sa, tma, x, (shared_e ? 0 : a.x * p.a_rows) + kTileM * t, full, pol_w);
           }
-          ptx::bulk_load(ptx::smem_u32(smem + kOffSfac + s * 16), sfa + g, 16, full);
           if (waited) {
             issue_b(g, s);
           } else {
@@ -231,36 +232,32 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    uint32_t it = 0;
-    int lt = 0;
-    bool ok = true;
-    for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
-      const int u = task / p.tiles;
-      const int4 a = __ldcg(act + u);
-      if (!task_valid(a, p)) continue;
-      const int nt = (a.z + 15) & ~15;
-      const int acc = lt & 1;
-      const uint32_t use = static_cast<uint32_t>(lt) >> 1;
-      ++lt;
-      if (!warp_wait(ptx::smem_u32(&bars->tempty[acc]), (use & 1) ^ 1, abort)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t d_tmem = tbase + acc * kAccCols;
-      for (int g = 0; g < G; ++g, ++it) {
-        const int s = it % kStages;
-        const uint32_t round = it / kStages;
-        if (!warp_wait(ptx::smem_u32(&bars->full[s]), round & 1, abort)) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      int lt = 0;
+      bool ok = true;
+      for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
+        const int u = task / p.tiles;
+        const int4 a = __ldcg(act + u);
+        if (!task_valid(a, p)) continue;
+        const int nt = (a.z + 15) & ~15;
+        const int acc = lt & 1;
+        const uint32_t use = static_cast<uint32_t>(lt) >> 1;
+        ++lt;
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->tempty[acc]), (use & 1) ^ 1, abort, kWaitLimitNs)) {
           ok = false;
           break;
         }
-        // the stage's weight-scale entry -> 32 identical 16-byte image rows
-        const uint4 cmp = *reinterpret_cast<const uint4*>(smem + kOffSfac + s * 16);
-        *reinterpret_cast<uint4*>(smem + kOffSfa + s * kImgBytes + lane * 16) = cmp;
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tbase + acc * kAccCols;
+        for (int g = 0; g < G; ++g, ++it) {
+          const int s = it % kStages;
+          const uint32_t round = it / kStages;
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[s]), round & 1, abort, kWaitLimitNs) ||
+              !ptx::mbar_wait(ptx::smem_u32(&bars->sfa_rdy[s]), round & 1, abort, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
           ptx::tc_fence_after();
           const uint32_t sf_a = tbase + kSfCol0 + s * 8;
           const uint32_t sf_b = sf_a + 4;
@@ -276,18 +273,47 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           }
           ptx::tc_commit(ptx::smem_u32(&bars->empty[s]));
         }
-        __syncwarp();
+        if (!ok) break;
+        ptx::tc_commit(ptx::smem_u32(&bars->tfull[acc]));
       }
-      if (!ok) break;
-      if (lane == 0) ptx::tc_commit(ptx::smem_u32(&bars->tfull[acc]));
-      __syncwarp();
-    }
-    // every MMA / copy this thread issued has completed once drain fires
-    if (lane == 0) {
+      // every MMA / copy this thread issued has completed once drain fires
       ptx::tc_commit(ptx::smem_u32(&bars->drain));
       drain_wait(ptx::smem_u32(&bars->drain), 0);
     }
     __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ weight-scale images
+    // Runs ahead of the MMA issuer: as soon as a ring slot is free it writes the
+    // slot's 32 x 16-byte image (the stage's 16-byte entry in every row).
+    uint32_t it = 0;
+    bool ok = true;
+    for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
+      const int u = task / p.tiles, t = task - u * p.tiles;
+      const int4 a = __ldcg(act + u);
+      if (!task_valid(a, p)) continue;
+      const uint4* sfa = p.sfa + (static_cast<size_t>(a.x) * p.tiles + t) * G;
+      const uint4 zero = make_uint4(0, 0, 0, 0);
+      const uint4 e0 = lane < G ? __ldg(sfa + lane) : zero;  // stages lane and lane + 32
+      const uint4 e1 = lane + 32 < G ? __ldg(sfa + lane + 32) : zero;
+      for (int g = 0; g < G; ++g, ++it) {
+        const int s = it % kStages;
+        const uint32_t round = it / kStages;
+        if (!warp_wait(ptx::smem_u32(&bars->empty[s]), (round & 1) ^ 1, abort)) {
+          ok = false;
+          break;
+        }
+        const uint4 src = g < 32 ? e0 : e1;
+        uint4 v;
+        v.x = __shfl_sync(0xffffffffu, src.x, g & 31);
+        v.y = __shfl_sync(0xffffffffu, src.y, g & 31);
+        v.z = __shfl_sync(0xffffffffu, src.z, g & 31);
+        v.w = __shfl_sync(0xffffffffu, src.w, g & 31);
+        *reinterpret_cast<uint4*>(smem + kOffSfa + s * kImgBytes + lane * 16) = v;
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->sfa_rdy[s]));
+      }
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp - 4;  // TMEM lane quarter

@@ -91,9 +91,9 @@ struct GatherParams {
 // B = gathered x8 rows, epilogue = SwiGLU + requant into h8 and the w2 scale
 // images. PHASE 2: A = w2 rows, B = h8 rows, epilogue = fp32 partial rows.
 struct ExpertParams {
-  CUtensorMap tm_a;         // routed experts' weight rows (2D view over all experts)
+  CUtensorMap tm_a;         // routed experts' weight rows (PHASE 13: 3D [expert half][row][col])
   CUtensorMap tm_a_shared;  // the shared expert's weight rows
-  CUtensorMap tm_b;         // activation rows (box: 16 rows x 128 bytes)
+  CUtensorMap tm_b[3];      // activation rows, boxes of 16 / 32 / 48 rows x 128 bytes
   const int* counters;
   const ActiveExpert* act;
   const uint4* sfa;         // [E + 1][tiles][G] compact weight-scale entries
