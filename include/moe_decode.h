@@ -232,16 +232,18 @@ void moe_destroy(moe_handle* h);
  *
  * Limits: 1 <= M <= 48; hidden a multiple of 128 in [256, 8192]; experts a
  * multiple of 32 in [32, 512]; 1 <= topk <= 16. A problem whose scratch
- * (logit partials, about 4 * 1024 * M bytes, plus small routing tables) would
- * not fit the array is refused with MOE_ERR_UNSUPPORTED before anything is
- * enqueued (e.g. experts = 512 with hidden > 4096). Other errors:
+ * (partial logits, 4 * KS * experts * M bytes with KS the router's K-split,
+ * about 1024 / experts and at least hidden / 1536, plus small routing tables)
+ * would not fit the array is refused with MOE_ERR_UNSUPPORTED before anything
+ * is enqueued (e.g. experts = 512 with hidden > 3072). Other errors:
  * MOE_ERR_ARG (null pointer), MOE_ERR_ALIGN (normed / gate_w not 16-byte
  * aligned, the others not 4-byte aligned), MOE_ERR_RANGE (M), MOE_ERR_CUDA.
  *
  * The first call on a device (with that device current) looks up the array's
  * device address and sets the kernel's shared-memory limit; make that first
- * call before any stream capture. Each call enqueues a memset of the array's
- * counters and one kernel on `stream` (void* holding a cudaStream_t). All
+ * call before any stream capture. Each call enqueues memsets of the array's
+ * counters and expert masks and two kernels on `stream` (void* holding a
+ * cudaStream_t). All
  * calls share the one array, which keeps the last call's contents: calls whose
  * work overlaps on the GPU (different streams, or concurrent host threads
  * without ordering) race on it and must be serialised by the caller.

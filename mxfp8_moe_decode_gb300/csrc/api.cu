@@ -32,6 +32,8 @@ struct moe_handle {
   uint8_t* x8;
   uint8_t* x8c;
   float* logit_part;
+  unsigned long long* mask;
+  int* ids;
   uint8_t* xg;
   uint8_t* h8;
   uint4* sfb13;
@@ -48,9 +50,9 @@ struct moe_handle {
 
 namespace {
 
-const char* const kKernelNames[] = {"seam", "router", "gather", "expert_w13", "expert_w2",
-                                    "combine"};
-constexpr int kNumKernels = 6;
+const char* const kKernelNames[] = {"seam",       "router",    "topk",   "gather",
+                                    "expert_w13", "expert_w2", "combine"};
+constexpr int kNumKernels = 7;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -219,12 +221,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
 
   const int H = cfg->hidden, E = cfg->experts, K = cfg->topk, I = cfg->inter;
   const int Mx = cfg->max_tokens;
-  // router K-split: about 128 CTAs, each slice <= 2048 columns, a multiple of 8
-  int ks = 128 / (E / kRouterWarps);
-  if (ks < 1) ks = 1;
-  if (ks > 16) ks = 16;
-  while (H / ks > 2048) ks *= 2;
-  while (H % (ks * 8)) ks /= 2;
+  const int ks = router_ksplit(H, E);
   h->ks = ks;
   h->hs = H / ks;
   h->rows_max = Mx * (K + 1);
@@ -247,6 +244,8 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   const size_t o_x8 = place(static_cast<size_t>(Mx) * H);
   const size_t o_x8c = place(static_cast<size_t>(Mx) * H / 32);
   const size_t o_lp = place(static_cast<size_t>(ks) * Mx * E * 4);
+  const size_t o_mk = place(static_cast<size_t>(E) * 8);
+  const size_t o_id = place(static_cast<size_t>(Mx) * K * 4);
   const size_t o_xg = place(static_cast<size_t>(h->rows_alloc) * H);
   const size_t o_h8 = place(static_cast<size_t>(h->rows_alloc) * I);
   const size_t o_s13 = place(static_cast<size_t>(h->units_max) * g13 * 512);
@@ -273,6 +272,8 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->x8 = b + o_x8;
   h->x8c = b + o_x8c;
   h->logit_part = reinterpret_cast<float*>(b + o_lp);
+  h->mask = reinterpret_cast<unsigned long long*>(b + o_mk);
+  h->ids = reinterpret_cast<int*>(b + o_id);
   h->xg = b + o_xg;
   h->h8 = b + o_h8;
   h->sfb13 = reinterpret_cast<uint4*>(b + o_s13);
@@ -396,22 +397,30 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   RouterParams rp;
   rp.normed = h->normed;
   rp.gate_w = static_cast<const __nv_bfloat16*>(h->w.gate_w);
-  rp.bias = h->w.bias;
   rp.logit_part = h->logit_part;
-  rp.counters = h->counters;
-  rp.act = h->act;
-  rp.route_w = h->route_w;
-  rp.tok_pos = h->tok_pos;
-  rp.pos_tok = h->pos_tok;
-  rp.dbg_ids = d.topk_ids;
-  rp.dbg_w = d.topk_w;
-  rp.dbg_logits = d.logits;
   rp.M = M;
   rp.H = H;
   rp.E = E;
-  rp.K = K;
   rp.KS = h->ks;
   rp.Hs = h->hs;
+
+  TopkParams tp;
+  tp.logit_part = h->logit_part;
+  tp.bias = h->w.bias;
+  tp.counters = h->counters;
+  tp.mask = h->mask;
+  tp.ids = h->ids;
+  tp.act = h->act;
+  tp.route_w = h->route_w;
+  tp.tok_pos = h->tok_pos;
+  tp.pos_tok = h->pos_tok;
+  tp.dbg_ids = d.topk_ids;
+  tp.dbg_w = d.topk_w;
+  tp.dbg_logits = d.logits;
+  tp.M = M;
+  tp.E = E;
+  tp.K = K;
+  tp.KS = h->ks;
 
   GatherParams gp;
   gp.x8 = h->x8;
@@ -442,14 +451,16 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   mark(1);
   if (err == cudaSuccess) err = launch_router(rp, st);
   mark(2);
-  if (err == cudaSuccess) err = launch_gather(gp, h->num_sms, st);
+  if (err == cudaSuccess) err = launch_topk(tp, st);
   mark(3);
-  if (err == cudaSuccess) err = launch_expert13(h->p13, h->num_sms, st);
+  if (err == cudaSuccess) err = launch_gather(gp, h->num_sms, st);
   mark(4);
-  if (err == cudaSuccess) err = launch_expert2(h->p2, h->num_sms, st);
+  if (err == cudaSuccess) err = launch_expert13(h->p13, h->num_sms, st);
   mark(5);
-  if (err == cudaSuccess) err = launch_combine(cp, st);
+  if (err == cudaSuccess) err = launch_expert2(h->p2, h->num_sms, st);
   mark(6);
+  if (err == cudaSuccess) err = launch_combine(cp, st);
+  mark(7);
   return cuda_code(err);
 }
 

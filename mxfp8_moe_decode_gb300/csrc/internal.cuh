@@ -31,7 +31,7 @@ constexpr int kErrBounds = 2;
 
 // counters region (int32 words at the start of the scratch)
 constexpr int kCtrErr = 0;       // device error word (bit set)
-constexpr int kCtrTicket = 1;    // router: CTAs done with their logits
+constexpr int kCtrTicket = 1;    // top-k: token CTAs done
 constexpr int kCtrUnits = 2;     // active experts this step (routed + 1 shared)
 constexpr int kCtrRouted = 3;    // distinct routed experts this step
 constexpr int kCtrWords = 64;
@@ -62,17 +62,24 @@ struct SeamParams {
 struct RouterParams {
   const __nv_bfloat16* normed;
   const __nv_bfloat16* gate_w;
-  const float* bias;
   float* logit_part;  // [KS][M][E]
+  int M, H, E, KS, Hs;
+};
+
+struct TopkParams {
+  const float* logit_part;    // [KS][M][E]
+  const float* bias;
   int* counters;
-  ActiveExpert* act;  // [E + 1]
-  float* route_w;     // [M][k]
-  int* tok_pos;       // [M][k + 1]: gathered row of (token, pick); pick k = shared
-  int* pos_tok;       // [M (k + 1)]: token of each gathered row
+  unsigned long long* mask;   // [E]: bit m set if token m picked the expert (zero between steps)
+  int* ids;                   // [M][k]
+  ActiveExpert* act;          // [E + 1]
+  float* route_w;             // [M][k]
+  int* tok_pos;               // [M][k + 1]: gathered row of (token, pick); pick k = shared
+  int* pos_tok;               // [M (k + 1)]: token of each gathered row
   int32_t* dbg_ids;
   float* dbg_w;
   float* dbg_logits;
-  int M, H, E, K, KS, Hs;
+  int M, E, K, KS;
 };
 
 struct GatherParams {
@@ -153,8 +160,10 @@ cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_seam(const SeamParams& p, int M, cudaStream_t s);
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 cudaError_t router_setup();
-size_t router_smem_bytes(int M, int Hs, int E);
+size_t router_smem_bytes(int M, int Hs);
+int router_ksplit(int hidden, int experts);
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_expert13(const ExpertParams& p, int grid, cudaStream_t s);
 cudaError_t launch_expert2(const ExpertParams& p, int grid, cudaStream_t s);

@@ -1,6 +1,6 @@
-// Allocation-free routing entry point: the router kernel (gate GEMV, sigmoid,
-// bias-adjusted top-k, normalised weights) run with its scratch in a fixed
-// file-scope device array instead of memory the library allocates.
+// Allocation-free routing entry point: the router kernels (gate GEMV, then
+// sigmoid, bias-adjusted top-k and normalised weights) run with their scratch
+// in a fixed file-scope device array instead of memory the library allocates.
 //
 // Who needs this: callers that may not allocate device memory at the time
 // they route. A serving engine that hands all GPU memory to its own pool, or
@@ -75,12 +75,7 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   if (experts % 32 || experts < 32 || experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (topk < 1 || topk > kMaxTopk || topk > experts) return MOE_ERR_UNSUPPORTED;
 
-  // the router's K-split: about 128 CTAs, slices <= 2048 columns
-  int ks = 128 / (experts / kRouterWarps);
-  if (ks < 1) ks = 1;
-  if (ks > 16) ks = 16;
-  while (hidden / ks > 2048) ks *= 2;
-  while (hidden % (ks * 8)) ks /= 2;
+  const int ks = router_ksplit(hidden, experts);
 
   // layout inside the static array; refuse problems that do not fit
   const size_t o_ctr = 0;
@@ -88,7 +83,9 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   const size_t o_rw = o_act + align256(static_cast<size_t>(experts + 1) * sizeof(ActiveExpert));
   const size_t o_tp = o_rw + align256(static_cast<size_t>(M) * topk * 4);
   const size_t o_pt = o_tp + align256(static_cast<size_t>(M) * (topk + 1) * 4);
-  const size_t o_lp = o_pt + align256(static_cast<size_t>(M) * (topk + 1) * 4);
+  const size_t o_mk = o_pt + align256(static_cast<size_t>(M) * (topk + 1) * 4);
+  const size_t o_id = o_mk + align256(static_cast<size_t>(experts) * 8);
+  const size_t o_lp = o_id + align256(static_cast<size_t>(M) * topk * 4);
   const size_t need = o_lp + align256(static_cast<size_t>(ks) * M * experts * 4);
   if (need > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;
 
@@ -103,32 +100,40 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   uint8_t* base = static_cast<uint8_t*>(base_v);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // the router's completion ticket (and error word) must start at zero; the
-  // array keeps whatever the previous call left
-  if (cudaMemsetAsync(base + o_ctr, 0, kCtrWords * 4, st) != cudaSuccess) {
+  // the top-k ticket, the error word and the expert masks must start at zero;
+  // the array keeps whatever the previous call left
+  if (cudaMemsetAsync(base + o_ctr, 0, kCtrWords * 4, st) != cudaSuccess ||
+      cudaMemsetAsync(base + o_mk, 0, static_cast<size_t>(experts) * 8, st) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
   RouterParams rp;
   rp.normed = static_cast<const __nv_bfloat16*>(normed);
   rp.gate_w = static_cast<const __nv_bfloat16*>(gate_w);
-  rp.bias = bias;
   rp.logit_part = reinterpret_cast<float*>(base + o_lp);
-  rp.counters = reinterpret_cast<int*>(base + o_ctr);
-  rp.act = reinterpret_cast<ActiveExpert*>(base + o_act);
-  rp.route_w = reinterpret_cast<float*>(base + o_rw);
-  rp.tok_pos = reinterpret_cast<int*>(base + o_tp);
-  rp.pos_tok = reinterpret_cast<int*>(base + o_pt);
-  rp.dbg_ids = topk_ids;
-  rp.dbg_w = topk_w;
-  rp.dbg_logits = nullptr;
   rp.M = M;
   rp.H = hidden;
   rp.E = experts;
-  rp.K = topk;
   rp.KS = ks;
   rp.Hs = hidden / ks;
-  if (launch_router(rp, st) != cudaSuccess) {
+  TopkParams tp;
+  tp.logit_part = rp.logit_part;
+  tp.bias = bias;
+  tp.counters = reinterpret_cast<int*>(base + o_ctr);
+  tp.mask = reinterpret_cast<unsigned long long*>(base + o_mk);
+  tp.ids = reinterpret_cast<int*>(base + o_id);
+  tp.act = reinterpret_cast<ActiveExpert*>(base + o_act);
+  tp.route_w = reinterpret_cast<float*>(base + o_rw);
+  tp.tok_pos = reinterpret_cast<int*>(base + o_tp);
+  tp.pos_tok = reinterpret_cast<int*>(base + o_pt);
+  tp.dbg_ids = topk_ids;
+  tp.dbg_w = topk_w;
+  tp.dbg_logits = nullptr;
+  tp.M = M;
+  tp.E = experts;
+  tp.K = topk;
+  tp.KS = ks;
+  if (launch_router(rp, st) != cudaSuccess || launch_topk(tp, st) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
