@@ -3,7 +3,7 @@
 
 Metric: microseconds per MoE decode step, with the achieved HBM GB/s of the
 dominant kernel against the measured copy bandwidth. A step is one pass of the
-whole path (seam, router, gather, w13 experts, w2 experts, combine) over one
+whole path (seam, router, top-k, gather, the experts, combine) over one
 batch of M synthetic token rows, replayed from a CUDA graph with every input
 resident in HBM; L2 is flushed (a 512 MB write) before every timed step.
 
@@ -272,12 +272,14 @@ def run_gpu(args):
     us_step = total_ms * 1e3 / (args.steps * world)
     names = kernel_names()
     alg = W.algorithmic_bytes(d, unique)
-    i13 = names.index("expert_w13")
-    w13_bytes = (unique + 1) * (2 * d.inter * d.hidden + (2 * d.inter // 32) * (d.hidden // 32))
-    ach = w13_bytes / (kmean[i13] * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "expert_w13", "achieved": round(ach, 1),
+    ix = names.index("experts")
+    # the expert kernel streams every touched expert (w13 + w2 + their scales) once
+    exp_bytes = (unique + 1) * d.expert_bytes()
+    ach = exp_bytes / (kmean[ix] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "experts", "achieved": round(ach, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "traffic": ncu_traffic("expert_w13"),
+                "traffic": ncu_traffic("experts"),
+                "alg_bytes_per_launch": exp_bytes,
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
                 if peaks["source"] == "measured" else "fallback 6.8 TB/s"}
     step_gbs = alg / (us_step * 1e-6) / 1e9 if world == 1 else None
@@ -322,13 +324,12 @@ def run_gpu(args):
             del g2
             us2 = statistics.mean(ms) * 1e3
             a2 = W.algorithmic_bytes(swl.dims, u2)
-            i2 = (u2 + 1) * (2 * swl.dims.inter * swl.dims.hidden
-                             + (2 * swl.dims.inter // 32) * (swl.dims.hidden // 32))
+            e2 = (u2 + 1) * swl.dims.expert_bytes()
             sweep[name] = {"M": swl.tokens, "us_per_step": round(us2, 2),
                            "unique_routed": u2, "alg_bytes": a2,
                            "step_gbs": round(a2 / (us2 * 1e-6) / 1e9, 1),
                            "step_frac": round(a2 / (us2 * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
-                           "w13_gbs": round(i2 / (km[i13] * 1e-3) / 1e9, 1),
+                           "experts_gbs": round(e2 / (km[ix] * 1e-3) / 1e9, 1),
                            "kernel_us": {n: round(k * 1e3, 2) for n, k in zip(names, km)}}
             L2.close()
             del L2

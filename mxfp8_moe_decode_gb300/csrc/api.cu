@@ -41,8 +41,8 @@ struct moe_handle {
   float* part;
   uint4* sfa13;
   uint4* sfa2;
-  ExpertParams p13;
-  ExpertParams p2;
+  ExpertParams pe;
+  int* ready;
   cudaEvent_t events[16];
   int n_events;
   cudaStream_t last_stream;
@@ -50,9 +50,8 @@ struct moe_handle {
 
 namespace {
 
-const char* const kKernelNames[] = {"seam",       "router",    "topk",   "gather",
-                                    "expert_w13", "expert_w2", "combine"};
-constexpr int kNumKernels = 7;
+const char* const kKernelNames[] = {"seam", "router", "topk", "gather", "experts", "combine"};
+constexpr int kNumKernels = 6;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -253,6 +252,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   const size_t o_pa = place(static_cast<size_t>(h->rows_max) * H * 4);
   const size_t o_a13 = place(static_cast<size_t>(E + 1) * t13 * g13 * 16);
   const size_t o_a2 = place(static_cast<size_t>(E + 1) * t2 * g2 * 16);
+  const size_t o_rd = place(static_cast<size_t>(E + 1) * 4);
   h->scratch_bytes = off;
 
   cudaError_t err = cudaMalloc(&h->scratch, h->scratch_bytes);
@@ -281,6 +281,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->part = reinterpret_cast<float*>(b + o_pa);
   h->sfa13 = reinterpret_cast<uint4*>(b + o_a13);
   h->sfa2 = reinterpret_cast<uint4*>(b + o_a2);
+  h->ready = reinterpret_cast<int*>(b + o_rd);
 
   err = cudaMemset(h->scratch, 0, h->scratch_bytes);
   if (err == cudaSuccess) err = router_setup();
@@ -307,45 +308,36 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
     return rc;
   }
 
-  // expert kernel parameter blocks (fixed for the handle's lifetime)
-  ExpertParams* ps[2] = {&h->p13, &h->p2};
-  for (ExpertParams* p : ps) {
-    p->counters = h->counters;
-    p->act = h->act;
-    p->err = h->counters + kCtrErr;
-    p->E = E;
-    p->inter = I;
-    p->hidden = H;
-    p->units_max = h->units_max;
-    p->rows_max = h->rows_max;
-  }
-  h->p13.sfa = h->sfa13;
-  h->p13.sfb = reinterpret_cast<const uint8_t*>(h->sfb13);
-  h->p13.h8 = h->h8;
-  h->p13.sfb_next = h->sfb2;
-  h->p13.part = nullptr;
-  h->p13.tiles = t13;
-  h->p13.G = g13;
-  h->p13.a_rows = 2 * I;
-  h->p13.next_G = g2;
-  h->p2.sfa = h->sfa2;
-  h->p2.sfb = h->sfb2;
-  h->p2.h8 = nullptr;
-  h->p2.sfb_next = nullptr;
-  h->p2.part = h->part;
-  h->p2.tiles = t2;
-  h->p2.G = g2;
-  h->p2.a_rows = H;
-  h->p2.next_G = 0;
+  // the expert kernel's parameter block (fixed for the handle's lifetime)
+  ExpertParams& pe = h->pe;
+  pe.counters = h->counters;
+  pe.act = h->act;
+  pe.sfa13 = h->sfa13;
+  pe.sfa2 = h->sfa2;
+  pe.sfb13 = reinterpret_cast<const uint8_t*>(h->sfb13);
+  pe.sfb2 = h->sfb2;
+  pe.h8 = h->h8;
+  pe.part = h->part;
+  pe.ready = h->ready;
+  pe.err = h->counters + kCtrErr;
+  pe.E = E;
+  pe.inter = I;
+  pe.hidden = H;
+  pe.t13 = t13;
+  pe.g13 = g13;
+  pe.t2 = t2;
+  pe.g2 = g2;
+  pe.units_max = h->units_max;
+  pe.rows_max = h->rows_max;
   // w13 as [2E halves][I rows][H]: one box = 64 gate rows over the 64 matching up rows
-  bool ok = encode_planes(&h->p13.tm_a, w->w13, H, I, 2ull * E, 64, 2) &&
-            encode_planes(&h->p13.tm_a_shared, w->sw13, H, I, 2, 64, 2) &&
-            encode_rows(&h->p2.tm_a, w->w2, I, static_cast<uint64_t>(E) * H, kTileM) &&
-            encode_rows(&h->p2.tm_a_shared, w->sw2, I, static_cast<uint64_t>(H), kTileM);
+  bool ok = encode_planes(&pe.tm_w13, w->w13, H, I, 2ull * E, 64, 2) &&
+            encode_planes(&pe.tm_w13_shared, w->sw13, H, I, 2, 64, 2) &&
+            encode_rows(&pe.tm_w2, w->w2, I, static_cast<uint64_t>(E) * H, kTileM) &&
+            encode_rows(&pe.tm_w2_shared, w->sw2, I, static_cast<uint64_t>(H), kTileM);
   for (int b = 0; b < 3 && ok; ++b) {
     const uint32_t rows = static_cast<uint32_t>(kBoxRows * (b + 1));
-    ok = encode_rows(&h->p13.tm_b[b], h->xg, H, h->rows_alloc, rows) &&
-         encode_rows(&h->p2.tm_b[b], h->h8, I, h->rows_alloc, rows);
+    ok = encode_rows(&pe.tm_x[b], h->xg, H, h->rows_alloc, rows) &&
+         encode_rows(&pe.tm_h[b], h->h8, I, h->rows_alloc, rows);
   }
   if (!ok) {
     cudaFree(h->scratch);
@@ -408,6 +400,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   tp.logit_part = h->logit_part;
   tp.bias = h->w.bias;
   tp.counters = h->counters;
+  tp.ready = h->ready;
   tp.mask = h->mask;
   tp.ids = h->ids;
   tp.act = h->act;
@@ -455,12 +448,10 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   mark(3);
   if (err == cudaSuccess) err = launch_gather(gp, h->num_sms, st);
   mark(4);
-  if (err == cudaSuccess) err = launch_expert13(h->p13, h->num_sms, st);
+  if (err == cudaSuccess) err = launch_experts(h->pe, h->num_sms, st);
   mark(5);
-  if (err == cudaSuccess) err = launch_expert2(h->p2, h->num_sms, st);
-  mark(6);
   if (err == cudaSuccess) err = launch_combine(cp, st);
-  mark(7);
+  mark(6);
   return cuda_code(err);
 }
 

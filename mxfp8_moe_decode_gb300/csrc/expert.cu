@@ -1,6 +1,6 @@
 // Grouped-expert kernel: block-scaled E4M3 GEMMs of the active experts on the
 // 5th-generation tensor cores (tcgen05, accumulators in TMEM), persistent over
-// the step's (expert, weight-tile) tasks.
+// the step's tasks -- first every w13 task, then every w2 task -- in one launch.
 //
 // "vllm.models.deepseek_v41.amd.mono.attention.device", mfma_scaled: the
 // expert GEMMs are block-scaled MMAs whose operands are both MX-FP8 with one
@@ -8,36 +8,40 @@
 // MonoLayerWeights: gate_up [2 inter, 5120] e4m3 with [2 inter / 32, 160]
 // E8M0 (32 x 32 blocks), down [5120, inter] with [160, inter / 32].
 //
-// Swap-AB: the weight rows are the MMA's M (128 per tile) and the expert's
+// Swap-AB: the weight rows are the MMA's M (128 per tile) and the unit's
 // tokens its N (rounded up to 16, at most 48), so the weights stream once
 // through shared memory while the few activation rows are reused from L2.
 //
-//  PHASE 13  task = (expert, 64 intermediate columns): A = the 64 gate rows
-//            over the matching 64 up rows of w13 (two TMA boxes), B = the
-//            expert's gathered MXFP8 token rows, K = H. Epilogue: silu(g) * u,
-//            requantised per token in 32-column groups (the same mx_code / E4M3
-//            rule as the seam) into h8 rows and the E8M0 images of the w2 pass.
-//  PHASE 2   task = (expert, 128 hidden rows): A = w2 rows, B = the expert's
-//            h8 rows, K = I. Epilogue: fp32 rows of y for the combine.
+//  w13 task = (unit, 64 intermediate columns): A = the 64 gate rows over the
+//    matching 64 up rows of w13 (one 3D TMA box), B = the unit's gathered
+//    MXFP8 token rows, K = H. Epilogue: silu(g) * u, requantised per token in
+//    32-column groups (the seam's mx_code / E4M3 rule) into h8 rows and the
+//    E8M0 images of the w2 tasks; then the unit's readiness counter +1.
+//  w2 task = (unit, 128 hidden rows): A = w2 rows, B = the unit's h8 rows,
+//    K = I. Its weight stages are issued at once; its activation stages wait
+//    (bounded) until all w13 tiles of the unit are done. Epilogue: fp32 rows
+//    of y for the combine.
+// Tasks are strided over the CTAs in that order, so every CTA finishes its
+// w13 tasks before any of its w2 tasks waits: the waits always end (all CTAs
+// of the grid, one per SM, are resident).
 //
 // Per CTA (one per SM, 256 threads): warp 0 lane 0 issues the TMA loads into
-// an 8-stage ring -- per stage one weight box (a w13 stage is one 3D box: the
-// 64 gate rows over the 64 matching up rows), one activation box (16 / 32 / 48
-// rows) and one bulk copy of the activation-scale image; weights evict-first
-// from L2. Warp 3 writes each stage's weight-scale image (the 16-byte entry of
-// the stage in all 32 rows tcgen05.cp expects) as soon as the slot is free.
-// Warp 1 lane 0 copies both scale images into TMEM and issues 4 MMAs (K = 32
-// each, the descriptor's scale-factor id picks the K block of the stage);
-// warp 2 owns the TMEM allocation; warps 4-7 drain the double-buffered
-// accumulator (each reads its 32-lane quarter). Every per-stage action is a
-// handful of single-thread instructions: at ~80 cycles per TMA or tcgen05
-// instruction, the issue cost per 16 KB stage sets the per-SM bandwidth. Every mbarrier wait is bounded; on a timeout the CTA
-// records kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
+// an 8-stage ring -- per stage one weight box, one activation box (16 / 32 /
+// 48 rows) and one bulk copy of the activation-scale image; weights
+// evict-first from L2. Warp 3 writes each stage's weight-scale image (the
+// stage's 16-byte entry in all 32 rows tcgen05.cp expects) as soon as the
+// slot is free. Warp 1 lane 0 copies both scale images into TMEM and issues 4
+// MMAs (K = 32 each, the descriptor's scale-factor id picks the K block of the
+// stage); warp 2 owns the TMEM allocation; warps 4-7 drain the double-buffered
+// accumulator (each reads its 32-lane quarter). At ~80 cycles per TMA or
+// tcgen05 instruction, the issue cost per 16 KB stage sets the per-SM
+// bandwidth, hence the few instructions per stage. Every mbarrier and
+// readiness wait is bounded; on a timeout the CTA records kErrTimeout, waits
+// for its own copies and MMAs, frees TMEM and exits.
 //
-// Launched with programmatic dependent launch: the prologue (barriers, TMEM,
-// descriptor prefetch) and the first task's weight stages run while the
-// previous kernel finishes; the activation operands and every global write
-// wait for it (griddepcontrol.wait).
+// Launched with programmatic dependent launch: the prologue and the first
+// task's weight stages run while the previous kernel finishes; activation
+// operands and every global write wait for it (griddepcontrol.wait).
 #include "internal.cuh"
 #include "mx.cuh"
 #include "ptx.cuh"
@@ -106,7 +110,51 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   ptx::mbar_wait(bar, parity, &never, kWaitLimitNs);
 }
 
-template <int PHASE>
+struct Task {
+  int phase;  // 0: w13, 1: w2
+  int u;      // unit (active expert)
+  int t;      // tile within the unit
+};
+
+__device__ __forceinline__ Task decode_task(int task, int n13, const ExpertParams& p) {
+  Task k;
+  if (task < n13) {
+    k.phase = 0;
+    k.u = task / p.t13;
+    k.t = task - k.u * p.t13;
+  } else {
+    const int j = task - n13;
+    k.phase = 1;
+    k.u = j / p.t2;
+    k.t = j - k.u * p.t2;
+  }
+  return k;
+}
+
+// Bounded wait until *ctr >= target (acquire, device scope); then the async
+// proxy (TMA) may read what the counting threads wrote.
+__device__ __forceinline__ bool wait_ready(const int* ctr, int target, volatile int* abort) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  if (v < target) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+      __nanosleep(64);
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      if (v >= target) break;
+      if ((i & 63) == 0) {
+        if (*abort) return false;
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+          *abort = 1;
+          return false;
+        }
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_constant__ ExpertParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -130,9 +178,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     misc->abort = 0;
     misc->epi_ok = 0;
     ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&p.tm_a);
-    ptx::prefetch_tmap(&p.tm_a_shared);
-    for (int b = 0; b < 3; ++b) ptx::prefetch_tmap(&p.tm_b[b]);
+    ptx::prefetch_tmap(&p.tm_w13);
+    ptx::prefetch_tmap(&p.tm_w13_shared);
+    ptx::prefetch_tmap(&p.tm_w2);
+    ptx::prefetch_tmap(&p.tm_w2_shared);
+    for (int b = 0; b < 3; ++b) {
+      ptx::prefetch_tmap(&p.tm_x[b]);
+      ptx::prefetch_tmap(&p.tm_h[b]);
+    }
   }
   if (warp == 2) {
     ptx::tmem_alloc(ptx::smem_u32(&misc->tmem_base), kTmemCols);
@@ -146,16 +199,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
   // reads anything this grid writes
   ptx::griddep_launch_dependents();
 
-  // The routing tables were written by the router, two kernels back: it has
-  // completed before this grid could launch (every kernel of the step waits
-  // for its predecessor before it lets the next one start). Read them past L1.
+  // The routing tables were written by the top-k kernel, two kernels back: it
+  // has completed before this grid could launch (every kernel of the step
+  // waits for its predecessor before it lets the next one start). Read them
+  // past L1.
   int units = __ldcg(p.counters + kCtrUnits);
   if (units < 0 || units > p.units_max) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
     units = 0;
   }
-  const int ntasks = units * p.tiles;
-  const int G = p.G;
+  const int n13 = units * p.t13;
+  const int ntasks = units * (p.t13 + p.t2);
   const int4* act = reinterpret_cast<const int4*>(p.act);
 
   if (warp == 0) {
@@ -165,21 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      // The first task's weight tiles (and their scale entries) do not depend
-      // on the previous kernel: they are issued for the whole ring before the
-      // grid-dependency wait; the activation halves of those stages follow it.
+      // Weight stages never depend on earlier work: they are issued at once.
+      // A task's activation stages are held back (at most one ring's worth)
+      // until the previous kernel is done (the first task) and, for a w2 task,
+      // until its unit's w13 tiles are done.
       bool waited = false;
-      int first_pending = 0, n_pending = 0;
       for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
-        const int u = task / p.tiles, t = task - u * p.tiles;
-        const int4 a = __ldcg(act + u);
+        const Task k = decode_task(task, n13, p);
+        const int4 a = __ldcg(act + k.u);
         if (!task_valid(a, p)) continue;
         const int nt = (a.z + 15) & ~15;
         const uint32_t bytes = kABytes + nt * kStageK + kImgBytes;
         const bool shared_e = a.x == p.E;
-        const CUtensorMap* tma = shared_e ? &p.tm_a_shared : &p.tm_a;
-        const CUtensorMap* tmb = &p.tm_b[nt / kBoxRows - 1];
-        const uint8_t* sfb = p.sfb + static_cast<size_t>(u) * G * kImgBytes;
+        const int G = k.phase ? p.g2 : p.g13;
+        const CUtensorMap* tmb = k.phase ? &p.tm_h[nt / kBoxRows - 1] : &p.tm_x[nt / kBoxRows - 1];
+        const uint8_t* sfb = k.phase ? p.sfb2 + static_cast<size_t>(k.u) * G * kImgBytes
+                                     : p.sfb13 + static_cast<size_t>(k.u) * G * kImgBytes;
         auto issue_b = [&](int g, int s) {
           const uint32_t full = ptx::smem_u32(&bars->full[s]);
           ptx::tma_load_2d(ptx::smem_u32(smem + kOffB + s * kBBytes), tmb, g * kStageK, a.y, full,
@@ -187,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           ptx::bulk_load(ptx::smem_u32(smem + kOffSfb + s * kImgBytes), sfb + g * kImgBytes,
                          kImgBytes, full);
         };
+        bool b_ok = waited && k.phase == 0;
+        int first_pending = 0, n_pending = 0;
         for (int g = 0; g < G; ++g, ++it) {
           const int s = it % kStages;
           const uint32_t round = it / kStages;
@@ -199,22 +256,36 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           ptx::mbar_arrive_expect_tx(full, bytes);
           const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
           const int x = g * kStageK;
-          if (PHASE == 13) {
+          if (k.phase == 0) {
             // one box: the 64 gate rows (half 2e) over the matching 64 up rows (half 2e + 1)
-            ptx::tma_load_3d(sa, tma, x, 64 * t, shared_e ? 0 : 2 * a.x, full, pol_w);
+            ptx::tma_load_3d(sa, shared_e ? &p.tm_w13_shared : &p.tm_w13, x, 64 * k.t,
+                             shared_e ? 0 : 2 * a.x, full, pol_w);
           } else {
-            ptx::tma_load_2d(sa, tma, x, (shared_e ? 0 : a.x * p.a_rows) + kTileM * t, full, pol_w);
+            ptx::tma_load_2d(sa, shared_e ? &p.tm_w2_shared : &p.tm_w2, x,
+                             (shared_e ? 0 : a.x * p.hidden) + kTileM * k.t, full, pol_w);
           }
-          if (waited) {
+          if (b_ok) {
             issue_b(g, s);
           } else {
-            if (n_pending == 0) first_pending = g;
+            if (n_pending == 0) first_pending = it;
             ++n_pending;
             if (n_pending == kStages || g == G - 1) {
-              ptx::griddep_wait();
-              waited = true;
-              for (int j = 0; j < n_pending; ++j) issue_b(first_pending + j, (first_pending + j) % kStages);
+              if (!waited) {
+                ptx::griddep_wait();
+                waited = true;
+              }
+              // on a timeout the held-back loads still go out (their data is
+              // not used), so that every issued stage completes before exit
+              if (k.phase == 1 && !wait_ready(p.ready + k.u, p.t13, abort)) ok = false;
+              b_ok = true;
+              const int g0 = g - (n_pending - 1);
+              for (int j = 0; j < n_pending; ++j)
+                issue_b(g0 + j, static_cast<int>((first_pending + j) % kStages));
               n_pending = 0;
+              if (!ok) {
+                ++it;  // count this stage for the drain below
+                break;
+              }
             }
           }
         }
@@ -237,10 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       int lt = 0;
       bool ok = true;
       for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
-        const int u = task / p.tiles;
-        const int4 a = __ldcg(act + u);
+        const Task k = decode_task(task, n13, p);
+        const int4 a = __ldcg(act + k.u);
         if (!task_valid(a, p)) continue;
         const int nt = (a.z + 15) & ~15;
+        const int G = k.phase ? p.g2 : p.g13;
         const int acc = lt & 1;
         const uint32_t use = static_cast<uint32_t>(lt) >> 1;
         ++lt;
@@ -266,10 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
           const uint32_t sb = ptx::smem_u32(smem + kOffB + s * kBBytes);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            ptx::tc_mma_mxf8(d_tmem, ptx::sdesc_k128_sw128(sa + 32 * k),
-                             ptx::sdesc_k128_sw128(sb + 32 * k), ptx::idesc_mxf8_e4m3(nt, k), sf_a,
-                             sf_b, (g | k) != 0);
+          for (int kk = 0; kk < 4; ++kk) {
+            ptx::tc_mma_mxf8(d_tmem, ptx::sdesc_k128_sw128(sa + 32 * kk),
+                             ptx::sdesc_k128_sw128(sb + 32 * kk), ptx::idesc_mxf8_e4m3(nt, kk), sf_a,
+                             sf_b, (g | kk) != 0);
           }
           ptx::tc_commit(ptx::smem_u32(&bars->empty[s]));
         }
@@ -288,10 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     uint32_t it = 0;
     bool ok = true;
     for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
-      const int u = task / p.tiles, t = task - u * p.tiles;
-      const int4 a = __ldcg(act + u);
+      const Task k = decode_task(task, n13, p);
+      const int4 a = __ldcg(act + k.u);
       if (!task_valid(a, p)) continue;
-      const uint4* sfa = p.sfa + (static_cast<size_t>(a.x) * p.tiles + t) * G;
+      const int G = k.phase ? p.g2 : p.g13;
+      const uint4* sfa = k.phase ? p.sfa2 + (static_cast<size_t>(a.x) * p.t2 + k.t) * G
+                                 : p.sfa13 + (static_cast<size_t>(a.x) * p.t13 + k.t) * G;
       const uint4 zero = make_uint4(0, 0, 0, 0);
       const uint4 e0 = lane < G ? __ldg(sfa + lane) : zero;  // stages lane and lane + 32
       const uint4 e1 = lane + 32 < G ? __ldg(sfa + lane + 32) : zero;
@@ -321,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     ptx::griddep_wait();  // before writing rows the previous kernels may read
     int lt = 0;
     for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
-      const int u = task / p.tiles, t = task - u * p.tiles;
-      const int4 a = __ldcg(act + u);
+      const Task k = decode_task(task, n13, p);
+      const int4 a = __ldcg(act + k.u);
       if (!task_valid(a, p)) continue;
       const int rows = a.z;
       const int nt = (rows + 15) & ~15;
@@ -345,11 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->tempty[acc]));
 
-      if (PHASE == 2) {
-        float* dst = p.part + static_cast<size_t>(a.y) * p.hidden + kTileM * t + 32 * q + lane;
+      if (k.phase == 1) {
+        float* dst = p.part + static_cast<size_t>(a.y) * p.hidden + kTileM * k.t + 32 * q + lane;
 #pragma unroll
         for (int n = 0; n < kMaxTokens; ++n)
           if (n < rows) dst[static_cast<size_t>(n) * p.hidden] = v[n];
+        epi_bar();
       } else {
         if (q >= 2) {
 #pragma unroll
@@ -358,11 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         }
         epi_bar();
         if (q < 2) {
-          const int i = 64 * t + 32 * q + lane;  // intermediate column
-          const int kb = i >> 5;                 // its 32-column block
+          const int i = 64 * k.t + 32 * q + lane;  // intermediate column
+          const int kb = i >> 5;                   // its 32-column block
           uint8_t* hrow = p.h8 + static_cast<size_t>(a.y) * p.inter + i;
-          uint8_t* img = p.sfb_next + (static_cast<size_t>(u) * p.next_G + (kb >> 2)) * kImgBytes +
-                         (kb & 3);
+          uint8_t* img = p.sfb2 + (static_cast<size_t>(k.u) * p.g2 + (kb >> 2)) * kImgBytes + (kb & 3);
 #pragma unroll
           for (int n = 0; n < kMaxTokens; ++n) {
             if (n < rows) {
@@ -378,9 +452,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
               if (lane == 0) img[(n & 31) * 16 + (n >> 5) * 4] = static_cast<uint8_t>(code);
             }
           }
+          // publish this tile's h8 columns and codes to the w2 tasks (their
+          // TMA reads them): fence, then the barrier, then one release count
+          __threadfence();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        epi_bar();
+        if (threadIdx.x == 128) {
+          __threadfence();
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.ready + k.u) : "memory");
         }
       }
-      epi_bar();
     }
   }
 
@@ -399,19 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
 size_t expert_smem_bytes(int) { return kSmemBytes; }
 
 cudaError_t expert_kernel_setup() {
-  cudaError_t e = cudaFuncSetAttribute(expert_kernel<13>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(expert_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSmemBytes));
 }
 
-cudaError_t launch_expert13(const ExpertParams& p, int grid, cudaStream_t s) {
-  return launch_pdl(expert_kernel<13>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
-}
-
-cudaError_t launch_expert2(const ExpertParams& p, int grid, cudaStream_t s) {
-  return launch_pdl(expert_kernel<2>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s) {
+  return launch_pdl(expert_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
 }
 
 }  // namespace moe

@@ -70,6 +70,7 @@ struct TopkParams {
   const float* logit_part;    // [KS][M][E]
   const float* bias;
   int* counters;
+  int* ready;                 // [E + 1] expert-kernel readiness counters to clear (or null)
   unsigned long long* mask;   // [E]: bit m set if token m picked the expert (zero between steps)
   int* ids;                   // [M][k]
   ActiveExpert* act;          // [E + 1]
@@ -94,30 +95,37 @@ struct GatherParams {
   int units_max, rows_max;
 };
 
-// The expert kernel's parameters. PHASE 13: A = w13 rows (gate + up halves),
-// B = gathered x8 rows, epilogue = SwiGLU + requant into h8 and the w2 scale
-// images. PHASE 2: A = w2 rows, B = h8 rows, epilogue = fp32 partial rows.
+// The grouped-expert kernel's parameters. One launch runs both GEMM phases:
+// first every (unit, w13 tile) task, then every (unit, w2 tile) task.
+//  w13 task = (unit, 64 intermediate columns): A = the 64 gate rows over the
+//    matching 64 up rows, B = the unit's gathered MXFP8 rows, K = H; epilogue:
+//    SwiGLU + requant into h8 rows and the w2 activation-scale images.
+//  w2 task = (unit, 128 hidden rows): A = w2 rows, B = the unit's h8 rows,
+//    K = I; epilogue: fp32 rows of y for the combine. It waits until all
+//    w13 tiles of its unit are done (the unit's readiness counter).
 struct ExpertParams {
-  CUtensorMap tm_a;         // routed experts' weight rows (PHASE 13: 3D [expert half][row][col])
-  CUtensorMap tm_a_shared;  // the shared expert's weight rows
-  CUtensorMap tm_b[3];      // activation rows, boxes of 16 / 32 / 48 rows x 128 bytes
+  CUtensorMap tm_w13;         // routed w13 as [2E halves][I rows][H] (3D)
+  CUtensorMap tm_w13_shared;  // shared w13 as [2 halves][I][H]
+  CUtensorMap tm_w2;          // routed w2 as [E H rows][I]
+  CUtensorMap tm_w2_shared;   // shared w2 [H][I]
+  CUtensorMap tm_x[3];        // gathered x8 rows, boxes of 16 / 32 / 48 rows x 128 bytes
+  CUtensorMap tm_h[3];        // h8 rows, same boxes
   const int* counters;
   const ActiveExpert* act;
-  const uint4* sfa;         // [E + 1][tiles][G] compact weight-scale entries
-  const uint8_t* sfb;       // [units][G][512] activation-scale images
-  uint8_t* h8;              // PHASE 13 out: [rows][I]
-  uint8_t* sfb_next;        // PHASE 13 out: [units][I/128][512] images of h8's codes
-  float* part;              // PHASE 2 out: [rows][H]
+  const uint4* sfa13;         // [E + 1][I/64][H/128] compact weight-scale entries
+  const uint4* sfa2;          // [E + 1][H/128][I/128]
+  const uint8_t* sfb13;       // [units][H/128][512] activation-scale images (gather)
+  uint8_t* sfb2;              // [units][I/128][512] images of h8's codes (w13 epilogue)
+  uint8_t* h8;                // [rows][I]
+  float* part;                // [rows][H]
+  int* ready;                 // [E + 1]: finished w13 tiles per unit (zeroed by the top-k kernel)
   int* err;
-  int E;        // routed experts (index E = shared)
-  int tiles;    // tiles per expert: I/64 (PHASE 13) or H/128 (PHASE 2)
-  int G;        // K stages per tile: H/128 (PHASE 13) or I/128 (PHASE 2)
-  int a_rows;   // rows of one routed expert's A matrix: 2I (PHASE 13) or H (PHASE 2)
-  int inter;    // I
-  int hidden;   // H
-  int next_G;   // PHASE 13: I/128 (groups of the w2 B operand)
-  int units_max;  // capacity of the active-expert table
-  int rows_max;   // capacity of the gathered rows
+  int E;                      // routed experts (index E = shared)
+  int inter, hidden;
+  int t13, g13;               // w13: tiles per unit (I/64), K stages (H/128)
+  int t2, g2;                 // w2: tiles per unit (H/128), K stages (I/128)
+  int units_max;              // capacity of the active-expert table
+  int rows_max;               // capacity of the gathered rows
 };
 
 struct CombineParams {
@@ -165,8 +173,7 @@ cudaError_t router_setup();
 size_t router_smem_bytes(int M, int Hs);
 int router_ksplit(int hidden, int experts);
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
-cudaError_t launch_expert13(const ExpertParams& p, int grid, cudaStream_t s);
-cudaError_t launch_expert2(const ExpertParams& p, int grid, cudaStream_t s);
+cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s);
 cudaError_t expert_kernel_setup();
 size_t expert_smem_bytes(int phase);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);

@@ -120,6 +120,7 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   tp.logit_part = rp.logit_part;
   tp.bias = bias;
   tp.counters = reinterpret_cast<int*>(base + o_ctr);
+  tp.ready = nullptr;
   tp.mask = reinterpret_cast<unsigned long long*>(base + o_mk);
   tp.ids = reinterpret_cast<int*>(base + o_id);
   tp.act = reinterpret_cast<ActiveExpert*>(base + o_act);

@@ -257,6 +257,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     p.mask[ex] = 0ull;  // ready for the next step
   }
   for (int i = tid; i < M * K; i += kTopkThreads) ids_s[i] = __ldcg(p.ids + i);
+  if (p.ready)  // the expert kernel's per-unit readiness counts start at zero
+    for (int u = tid; u <= E; u += kTopkThreads) p.ready[u] = 0;
   __syncthreads();
 
   // ---- warp 0: active experts in increasing id, their row runs
