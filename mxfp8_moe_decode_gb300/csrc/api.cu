@@ -20,7 +20,7 @@ struct moe_handle {
   int device;
   int num_sms;
   int ks, hs;
-  int units_max, rows_max, rows_alloc;
+  int units_max, rows_max;
   uint8_t* scratch;
   size_t scratch_bytes;
   int* counters;
@@ -34,10 +34,8 @@ struct moe_handle {
   float* logit_part;
   unsigned long long* mask;
   int* ids;
-  uint8_t* xg;
-  uint8_t* h8;
-  uint4* sfb13;
-  uint8_t* sfb2;
+  uint8_t* xpan;
+  uint8_t* hpan;
   float* part;
   uint4* sfa13;
   uint4* sfa2;
@@ -167,12 +165,12 @@ int moe_scratch_region(const moe_handle* h, int region, void** ptr, size_t* byte
   const size_t H = h->cfg.hidden, I = h->cfg.inter, K = h->cfg.topk;
   switch (region) {
     case MOE_REGION_GATHERED:
-      *ptr = h->xg;
-      *bytes = static_cast<size_t>(h->rows_max) * H;
+      *ptr = h->xpan;
+      *bytes = static_cast<size_t>(h->units_max) * (H / 128) * kPanelPitch;
       return MOE_OK;
     case MOE_REGION_H8:
-      *ptr = h->h8;
-      *bytes = static_cast<size_t>(h->rows_max) * I;
+      *ptr = h->hpan;
+      *bytes = static_cast<size_t>(h->units_max) * (I / 128) * kPanelPitch;
       return MOE_OK;
     case MOE_REGION_PARTIAL:
       *ptr = h->part;
@@ -224,7 +222,6 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->ks = ks;
   h->hs = H / ks;
   h->rows_max = Mx * (K + 1);
-  h->rows_alloc = h->rows_max + kMaxTokens;
   h->units_max = (E < Mx * K ? E : Mx * K) + 1;
   const int g13 = H / 128, g2 = I / 128, t13 = I / 64, t2 = H / 128;
 
@@ -245,10 +242,8 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   const size_t o_lp = place(static_cast<size_t>(ks) * Mx * E * 4);
   const size_t o_mk = place(static_cast<size_t>(E) * 8);
   const size_t o_id = place(static_cast<size_t>(Mx) * K * 4);
-  const size_t o_xg = place(static_cast<size_t>(h->rows_alloc) * H);
-  const size_t o_h8 = place(static_cast<size_t>(h->rows_alloc) * I);
-  const size_t o_s13 = place(static_cast<size_t>(h->units_max) * g13 * 512);
-  const size_t o_s2 = place(static_cast<size_t>(h->units_max) * g2 * 512);
+  const size_t o_xp = place(static_cast<size_t>(h->units_max) * g13 * kPanelPitch);
+  const size_t o_hp = place(static_cast<size_t>(h->units_max) * g2 * kPanelPitch);
   const size_t o_pa = place(static_cast<size_t>(h->rows_max) * H * 4);
   const size_t o_a13 = place(static_cast<size_t>(E + 1) * t13 * g13 * 16);
   const size_t o_a2 = place(static_cast<size_t>(E + 1) * t2 * g2 * 16);
@@ -274,10 +269,8 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->logit_part = reinterpret_cast<float*>(b + o_lp);
   h->mask = reinterpret_cast<unsigned long long*>(b + o_mk);
   h->ids = reinterpret_cast<int*>(b + o_id);
-  h->xg = b + o_xg;
-  h->h8 = b + o_h8;
-  h->sfb13 = reinterpret_cast<uint4*>(b + o_s13);
-  h->sfb2 = b + o_s2;
+  h->xpan = b + o_xp;
+  h->hpan = b + o_hp;
   h->part = reinterpret_cast<float*>(b + o_pa);
   h->sfa13 = reinterpret_cast<uint4*>(b + o_a13);
   h->sfa2 = reinterpret_cast<uint4*>(b + o_a2);
@@ -314,9 +307,8 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   pe.act = h->act;
   pe.sfa13 = h->sfa13;
   pe.sfa2 = h->sfa2;
-  pe.sfb13 = reinterpret_cast<const uint8_t*>(h->sfb13);
-  pe.sfb2 = h->sfb2;
-  pe.h8 = h->h8;
+  pe.xpan = h->xpan;
+  pe.hpan = h->hpan;
   pe.part = h->part;
   pe.ready = h->ready;
   pe.err = h->counters + kCtrErr;
@@ -334,11 +326,6 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
             encode_planes(&pe.tm_w13_shared, w->sw13, H, I, 2, 64, 2) &&
             encode_rows(&pe.tm_w2, w->w2, I, static_cast<uint64_t>(E) * H, kTileM) &&
             encode_rows(&pe.tm_w2_shared, w->sw2, I, static_cast<uint64_t>(H), kTileM);
-  for (int b = 0; b < 3 && ok; ++b) {
-    const uint32_t rows = static_cast<uint32_t>(kBoxRows * (b + 1));
-    ok = encode_rows(&pe.tm_x[b], h->xg, H, h->rows_alloc, rows) &&
-         encode_rows(&pe.tm_h[b], h->h8, I, h->rows_alloc, rows);
-  }
   if (!ok) {
     cudaFree(h->scratch);
     delete h;
@@ -421,8 +408,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   gp.counters = h->counters;
   gp.act = h->act;
   gp.pos_tok = h->pos_tok;
-  gp.xg = h->xg;
-  gp.sfb13 = h->sfb13;
+  gp.xpan = h->xpan;
   gp.M = M;
   gp.H = H;
   gp.K = K;

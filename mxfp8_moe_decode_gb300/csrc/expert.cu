@@ -13,11 +13,12 @@
 // through shared memory while the few activation rows are reused from L2.
 //
 //  w13 task = (unit, 64 intermediate columns): A = the 64 gate rows over the
-//    matching 64 up rows of w13 (one 3D TMA box), B = the unit's gathered
-//    MXFP8 token rows, K = H. Epilogue: silu(g) * u, requantised per token in
-//    32-column groups (the seam's mx_code / E4M3 rule) into h8 rows and the
-//    E8M0 images of the w2 tasks; then the unit's readiness counter +1.
-//  w2 task = (unit, 128 hidden rows): A = w2 rows, B = the unit's h8 rows,
+//    matching 64 up rows of w13 (one 3D TMA box), B = the unit's MXFP8 token
+//    rows (its x panels, written by the gather), K = H. Epilogue: silu(g) * u,
+//    requantised per token in 32-column groups (the seam's mx_code / E4M3
+//    rule) straight into the unit's h panels (rows and scale images); then
+//    the unit's readiness counter +1.
+//  w2 task = (unit, 128 hidden rows): A = w2 rows, B = the unit's h panels,
 //    K = I. Its weight stages are issued at once; its activation stages wait
 //    (bounded) until all w13 tiles of the unit are done. Epilogue: fp32 rows
 //    of y for the combine.
@@ -25,10 +26,10 @@
 // w13 tasks before any of its w2 tasks waits: the waits always end (all CTAs
 // of the grid, one per SM, are resident).
 //
-// Per CTA (one per SM, 256 threads): warp 0 lane 0 issues the TMA loads into
-// an 8-stage ring -- per stage one weight box, one activation box (16 / 32 /
-// 48 rows) and one bulk copy of the activation-scale image; weights
-// evict-first from L2. Warp 3 writes each stage's weight-scale image (the
+// Per CTA (one per SM, 256 threads): warp 0 lane 0 issues the loads into an
+// 8-stage ring -- per stage one weight box (TMA, evict-first from L2) and one
+// contiguous bulk copy of the activation panel (rows + scale image, already
+// in the swizzled layout the MMA reads, evict-last). Warp 3 writes each stage's weight-scale image (the
 // stage's 16-byte entry in all 32 rows tcgen05.cp expects) as soon as the
 // slot is free. Warp 1 lane 0 copies both scale images into TMEM and issues 4
 // MMAs (K = 32 each, the descriptor's scale-factor id picks the K block of the
@@ -51,13 +52,12 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr uint32_t kABytes = kTileM * kStageK;           // 16 KB
-constexpr uint32_t kBBytes = kMaxTokens * kStageK;       // 6 KB
 constexpr uint32_t kImgBytes = 32 * 16;                  // scale image of one stage
+constexpr uint32_t kBBytes = 7 * 1024;  // one activation panel (<= 48 rows + image), 1024-aligned
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
-constexpr uint32_t kOffSfb = kOffSfa + kStages * kImgBytes;
-constexpr uint32_t kOffXchg = kOffSfb + kStages * kImgBytes;
+constexpr uint32_t kOffXchg = kOffSfa + kStages * kImgBytes;
 constexpr uint32_t kOffBar = kOffXchg + kMaxTokens * 64 * 4;
 constexpr uint32_t kOffMisc = kOffBar + 256;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
@@ -67,12 +67,13 @@ constexpr uint32_t kAccCols = 64;
 constexpr uint32_t kSfCol0 = 128;
 
 static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "B tiles must stay 1024-aligned");
+static_assert(kBBytes >= kPanelPitch, "a panel fits its slot");
 static_assert(kOffSfa % 512 == 0, "scale images alignment");
 static_assert(kSfCol0 + kStages * 8 <= kTmemCols, "TMEM budget");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Bars {
-  uint64_t full[kStages];     // weights + activations + activation scales landed
+  uint64_t full[kStages];     // weights + activation panel landed
   uint64_t empty[kStages];    // the stage's MMAs (and scale copies) completed
   uint64_t sfa_rdy[kStages];  // the stage's weight-scale image is written
   uint64_t tfull[2];
@@ -182,10 +183,6 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     ptx::prefetch_tmap(&p.tm_w13_shared);
     ptx::prefetch_tmap(&p.tm_w2);
     ptx::prefetch_tmap(&p.tm_w2_shared);
-    for (int b = 0; b < 3; ++b) {
-      ptx::prefetch_tmap(&p.tm_x[b]);
-      ptx::prefetch_tmap(&p.tm_h[b]);
-    }
   }
   if (warp == 2) {
     ptx::tmem_alloc(ptx::smem_u32(&misc->tmem_base), kTmemCols);
@@ -229,18 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         const int4 a = __ldcg(act + k.u);
         if (!task_valid(a, p)) continue;
         const int nt = (a.z + 15) & ~15;
-        const uint32_t bytes = kABytes + nt * kStageK + kImgBytes;
+        const uint32_t pbytes = nt * 128 + kImgBytes;  // the panel's used part
+        const uint32_t bytes = kABytes + pbytes;
         const bool shared_e = a.x == p.E;
         const int G = k.phase ? p.g2 : p.g13;
-        const CUtensorMap* tmb = k.phase ? &p.tm_h[nt / kBoxRows - 1] : &p.tm_x[nt / kBoxRows - 1];
-        const uint8_t* sfb = k.phase ? p.sfb2 + static_cast<size_t>(k.u) * G * kImgBytes
-                                     : p.sfb13 + static_cast<size_t>(k.u) * G * kImgBytes;
+        const uint8_t* pan = (k.phase ? p.hpan : p.xpan) + static_cast<size_t>(k.u) * G * kPanelPitch;
         auto issue_b = [&](int g, int s) {
-          const uint32_t full = ptx::smem_u32(&bars->full[s]);
-          ptx::tma_load_2d(ptx::smem_u32(smem + kOffB + s * kBBytes), tmb, g * kStageK, a.y, full,
-                           pol_x);
-          ptx::bulk_load(ptx::smem_u32(smem + kOffSfb + s * kImgBytes), sfb + g * kImgBytes,
-                         kImgBytes, full);
+          ptx::bulk_load(ptx::smem_u32(smem + kOffB + s * kBBytes), pan + g * kPanelPitch, pbytes,
+                         ptx::smem_u32(&bars->full[s]), pol_x);
         };
         bool b_ok = waited && k.phase == 0;
         int first_pending = 0, n_pending = 0;
@@ -333,10 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           ptx::tc_fence_after();
           const uint32_t sf_a = tbase + kSfCol0 + s * 8;
           const uint32_t sf_b = sf_a + 4;
-          ptx::tc_cp_32x128b_x4(sf_a, ptx::sdesc_rows16(ptx::smem_u32(smem + kOffSfa + s * kImgBytes)));
-          ptx::tc_cp_32x128b_x4(sf_b, ptx::sdesc_rows16(ptx::smem_u32(smem + kOffSfb + s * kImgBytes)));
           const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
           const uint32_t sb = ptx::smem_u32(smem + kOffB + s * kBBytes);
+          ptx::tc_cp_32x128b_x4(sf_a, ptx::sdesc_rows16(ptx::smem_u32(smem + kOffSfa + s * kImgBytes)));
+          ptx::tc_cp_32x128b_x4(sf_b, ptx::sdesc_rows16(sb + nt * 128));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             ptx::tc_mma_mxf8(d_tmem, ptx::sdesc_k128_sw128(sa + 32 * kk),
@@ -435,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         if (q < 2) {
           const int i = 64 * k.t + 32 * q + lane;  // intermediate column
           const int kb = i >> 5;                   // its 32-column block
-          uint8_t* hrow = p.h8 + static_cast<size_t>(a.y) * p.inter + i;
-          uint8_t* img = p.sfb2 + (static_cast<size_t>(k.u) * p.g2 + (kb >> 2)) * kImgBytes + (kb & 3);
+          uint8_t* panel = p.hpan + (static_cast<size_t>(k.u) * p.g2 + (i >> 7)) * kPanelPitch;
+          uint8_t* img = panel + nt * 128 + (kb & 3);
 #pragma unroll
           for (int n = 0; n < kMaxTokens; ++n) {
             if (n < rows) {
@@ -448,12 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
               for (int off = 16; off > 0; off >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
               const int code = mx_code(amax);
-              hrow[static_cast<size_t>(n) * p.inter] = e4m3(clamp_e4m3(h * mx_mul(code)));
+              panel[panel_byte(n, i & 127)] = e4m3(clamp_e4m3(h * mx_mul(code)));
               if (lane == 0) img[(n & 31) * 16 + (n >> 5) * 4] = static_cast<uint8_t>(code);
             }
           }
           // publish this tile's h8 columns and codes to the w2 tasks (their
-          // TMA reads them): fence, then the barrier, then one release count
+          // bulk copies read them): fence, then the barrier, then one release count
           __threadfence();
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }

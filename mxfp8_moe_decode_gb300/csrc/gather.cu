@@ -1,14 +1,14 @@
 // Operand staging for the expert kernel.
 //
-// gather_kernel (every step): copies each token's MXFP8 row into the gathered
-// activation rows, one contiguous run per active expert (the order the router
-// chose), and writes each active expert's activation-scale images: for every
-// 128-column K stage a 32 x 16-byte matrix whose row r holds, in 32-bit cell
-// c, the four E8M0 codes (4 consecutive 32-column blocks) of the expert's
-// token 32 c + r (zero past its token count). That is the layout the block-
-// scaled MMA reads from TMEM (row n of the operand at TMEM lane n % 32,
-// column n / 32; byte b of a cell = K block b of the stage), copied there by
-// tcgen05.cp.
+// gather_kernel (every step): builds each active expert's activation panels
+// (the layout is described beside kPanelPitch): for every 128-column K stage,
+// the expert's MXFP8 token rows (the order the router chose) as the 128-byte
+// swizzled image the MMA reads, then the stage's scale image -- row r holds in
+// 32-bit cell j the four E8M0 codes (4 consecutive 32-column blocks) of the
+// expert's token 32 j + r, zero past its token count. That image is the layout
+// the block-scaled MMA reads from TMEM (row n of the operand at TMEM lane
+// n % 32, column n / 32; byte b of a cell = K block b of the stage), copied
+// there by tcgen05.cp.
 //
 // sfa_pack_kernel (once, at handle creation): the weights' 32 x 32-block E8M0
 // codes ("vllm.models.deepseek_v41.amd.mono.runner", MonoLayerWeights.check:
@@ -23,43 +23,67 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMaxRows = kMaxTokens * (kMaxTopk + 1);
+static_assert(kMaxTokens <= 64, "scale images use cells 0 and 1 only");
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p) {
+  // gathered row -> (unit << 16) | (row within the unit << 8) | the unit's padded rows
+  __shared__ uint32_t row_map[kMaxRows];
+  constexpr uint32_t kNone = 0xffffffffu;
+  const int H = p.H, G = p.G;
+  const int rows = min(p.M * (p.K + 1), min(p.rows_max, kMaxRows));
+  for (int i = threadIdx.x; i < rows; i += kThreads) row_map[i] = kNone;
   ptx::griddep_wait();  // routing tables and x8 come from the previous kernels
   ptx::griddep_launch_dependents();
-  const int H = p.H;
-  const int rows = p.M * (p.K + 1);
+  int units = p.counters[kCtrUnits];
+  if (units < 0 || units > p.units_max) units = 0;  // the expert kernel reports it
+  __syncthreads();
+  for (int u = threadIdx.x; u < units; u += kThreads) {
+    const int4 a = *reinterpret_cast<const int4*>(p.act + u);  // expert, first row, rows, pad
+    if (a.y < 0 || a.z < 1 || a.z > kMaxTokens || a.y + a.z > rows) continue;
+    const uint32_t nt = static_cast<uint32_t>((a.z + 15) & ~15);
+    for (int r = 0; r < a.z; ++r)
+      row_map[a.y + r] = (static_cast<uint32_t>(u) << 16) | (static_cast<uint32_t>(r) << 8) | nt;
+  }
+  __syncthreads();
+
+  // token rows: one 16-byte chunk per thread and step
   const int n16 = H >> 4;
   const long long stride = static_cast<long long>(gridDim.x) * kThreads;
   const long long start = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   for (long long i = start; i < static_cast<long long>(rows) * n16; i += stride) {
     const int row = static_cast<int>(i / n16);
     const int c = static_cast<int>(i - static_cast<long long>(row) * n16);
+    const uint32_t map = row_map[row];
     const int m = p.pos_tok[row];
-    reinterpret_cast<uint4*>(p.xg + static_cast<size_t>(row) * H)[c] =
+    if (map == kNone || m < 0 || m >= p.M) continue;
+    const int u = static_cast<int>(map >> 16), r = static_cast<int>((map >> 8) & 255u);
+    uint8_t* panel = p.xpan + (static_cast<size_t>(u) * G + (c >> 3)) * kPanelPitch;
+    *reinterpret_cast<uint4*>(panel + panel_byte(r, (c & 7) << 4)) =
         reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H)[c];
   }
-  int units = p.counters[kCtrUnits];
-  if (units < 0 || units > p.units_max) units = 0;  // the expert kernel reports it
-  const int G = p.G;
+
+  // scale images: one 16-byte image row per thread and step
   const int cstride = H >> 5;  // codes per token row
   for (long long i = start; i < static_cast<long long>(units) * G * 32; i += stride) {
     const int r = static_cast<int>(i & 31);
     const long long ug = i >> 5;
     const int g = static_cast<int>(ug % G);
     const int u = static_cast<int>(ug / G);
-    const int4 a = *reinterpret_cast<const int4*>(p.act + u);  // expert, pos_base, rows, pad
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (a.y < 0 || a.z < 0 || a.z > kMaxTokens || a.y + a.z > p.rows_max) continue;
-    if (r < a.z) {
-      const int m = p.pos_tok[a.y + r];
-      v.x = *reinterpret_cast<const uint32_t*>(p.x8c + static_cast<size_t>(m) * cstride + 4 * g);
+    const int4 a = *reinterpret_cast<const int4*>(p.act + u);
+    if (a.y < 0 || a.z < 1 || a.z > kMaxTokens || a.y + a.z > rows) continue;
+    const int nt = (a.z + 15) & ~15;
+    uint32_t cell[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (32 * j + r < a.z) {
+        const int m = p.pos_tok[a.y + 32 * j + r];
+        if (m >= 0 && m < p.M)
+          cell[j] = *reinterpret_cast<const uint32_t*>(p.x8c + static_cast<size_t>(m) * cstride + 4 * g);
+      }
     }
-    if (32 + r < a.z) {
-      const int m = p.pos_tok[a.y + 32 + r];
-      v.y = *reinterpret_cast<const uint32_t*>(p.x8c + static_cast<size_t>(m) * cstride + 4 * g);
-    }
-    p.sfb13[i] = v;
+    uint8_t* panel = p.xpan + (static_cast<size_t>(u) * G + g) * kPanelPitch;
+    *reinterpret_cast<uint4*>(panel + nt * 128 + r * 16) = make_uint4(cell[0], cell[1], 0u, 0u);
   }
 }
 

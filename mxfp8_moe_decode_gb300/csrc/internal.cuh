@@ -18,7 +18,6 @@ namespace moe {
 constexpr int kMaxTokens = 48;     // the pages' MAX_TOKENS; also the largest MMA N used
 constexpr int kMaxTopk = 16;
 constexpr int kMaxExperts = 512;
-constexpr int kBoxRows = 16;       // TMA box height of the activation (B) operand
 constexpr int kStages = 8;         // smem ring depth of the expert kernel
 constexpr int kTileM = 128;        // MMA M: weight rows per tile
 constexpr int kStageK = 128;       // K bytes per stage (one 128-byte swizzle row)
@@ -83,14 +82,32 @@ struct TopkParams {
   int M, E, K, KS;
 };
 
+// Activation panels. The B operand of one K stage of one unit is stored as the
+// exact shared-memory image the MMA reads, followed by its scale image, so that
+// one contiguous bulk copy stages both:
+//   bytes [0, nt * 128): the unit's rows (nt = rows rounded up to 16), 128 bytes
+//     of K each, 128-byte swizzled: the 16-byte chunk c of row r sits at chunk
+//     c ^ (r % 8) of that row (the layout a 128B-swizzle TMA box writes);
+//   bytes [nt * 128, nt * 128 + 512): 32 rows x 16 bytes, row r holding in its
+//     32-bit cell j the four E8M0 codes of the stage's K blocks for token 32 j + r.
+// Panels sit at a fixed pitch: panel (u, g) at ((u * G + g) * kPanelPitch).
+// Rows past a unit's token count hold stale finite data: the MMA output column
+// of such a row depends on that row alone and is never read.
+constexpr uint32_t kPanelPitch = kMaxTokens * 128 + 512;
+static_assert(kPanelPitch % 16 == 0, "bulk copies need 16-byte multiples");
+
+__host__ __device__ __forceinline__ uint32_t panel_byte(int r, int k) {
+  return static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(k >> 4) ^ (r & 7)) << 4) +
+         static_cast<uint32_t>(k & 15);
+}
+
 struct GatherParams {
   const uint8_t* x8;
   const uint8_t* x8c;
   const int* counters;
   const ActiveExpert* act;
   const int* pos_tok;
-  uint8_t* xg;     // [rows][H]
-  uint4* sfb13;    // [units][H/128][32] 16-byte image rows
+  uint8_t* xpan;   // [units][H/128] panels of the units' x8 rows
   int M, H, K, G;  // G = H / 128
   int units_max, rows_max;
 };
@@ -108,15 +125,12 @@ struct ExpertParams {
   CUtensorMap tm_w13_shared;  // shared w13 as [2 halves][I][H]
   CUtensorMap tm_w2;          // routed w2 as [E H rows][I]
   CUtensorMap tm_w2_shared;   // shared w2 [H][I]
-  CUtensorMap tm_x[3];        // gathered x8 rows, boxes of 16 / 32 / 48 rows x 128 bytes
-  CUtensorMap tm_h[3];        // h8 rows, same boxes
   const int* counters;
   const ActiveExpert* act;
   const uint4* sfa13;         // [E + 1][I/64][H/128] compact weight-scale entries
   const uint4* sfa2;          // [E + 1][H/128][I/128]
-  const uint8_t* sfb13;       // [units][H/128][512] activation-scale images (gather)
-  uint8_t* sfb2;              // [units][I/128][512] images of h8's codes (w13 epilogue)
-  uint8_t* h8;                // [rows][I]
+  const uint8_t* xpan;        // [units][H/128] panels of x8 rows (written by the gather)
+  uint8_t* hpan;              // [units][I/128] panels of h8 rows (written by the w13 epilogue)
   float* part;                // [rows][H]
   int* ready;                 // [E + 1]: finished w13 tiles per unit (zeroed by the top-k kernel)
   int* err;

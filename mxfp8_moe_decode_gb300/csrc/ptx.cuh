@@ -137,6 +137,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// The same with an L2 cache-eviction policy for the source lines.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy
 // (tcgen05.cp / tcgen05.mma / TMA) of this CTA.
 __device__ __forceinline__ void fence_proxy_async_smem() {
