@@ -312,6 +312,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   pe.part = h->part;
   pe.ready = h->ready;
   pe.err = h->counters + kCtrErr;
+  pe.task_ctr = h->counters + kCtrTasks;
   pe.E = E;
   pe.inter = I;
   pe.hidden = H;

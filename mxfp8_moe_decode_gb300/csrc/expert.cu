@@ -22,9 +22,12 @@
 //    K = I. Its weight stages are issued at once; its activation stages wait
 //    (bounded) until all w13 tiles of the unit are done. Epilogue: fp32 rows
 //    of y for the combine.
-// Tasks are strided over the CTAs in that order, so every CTA finishes its
-// w13 tasks before any of its w2 tasks waits: the waits always end (all CTAs
-// of the grid, one per SM, are resident).
+// Tasks are handed out in that order from a global counter: a CTA's producer
+// takes the next id when it starts a task and passes the ids on to the CTA's
+// other roles through a small queue in shared memory. Every w13 task is handed
+// out before any w2 task, to a CTA that finishes it without waiting on
+// anything, so the readiness waits always end (all CTAs of the grid, one per
+// SM, are resident).
 //
 // Per CTA (one per SM, 256 threads): warp 0 lane 0 issues the loads into an
 // 8-stage ring -- per stage one weight box (TMA, evict-first from L2) and one
@@ -59,12 +62,13 @@ constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffXchg = kOffSfa + kStages * kImgBytes;
 constexpr uint32_t kOffBar = kOffXchg + kMaxTokens * 64 * 4;
-constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 constexpr uint32_t kTmemCols = 256;  // 2 accumulators x 64 + 8 stages x 8 scale columns
 constexpr uint32_t kAccCols = 64;
 constexpr uint32_t kSfCol0 = 128;
+constexpr int kTaskSlots = 8;  // task-id queue from the producer to the other roles
 
 static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "B tiles must stay 1024-aligned");
 static_assert(kBBytes >= kPanelPitch, "a panel fits its slot");
@@ -79,14 +83,19 @@ struct Bars {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t task_full[kTaskSlots];   // the producer posted a task id
+  uint64_t task_empty[kTaskSlots];  // the MMA issuer, the helper warp and the epilogue read it
 };
-static_assert(sizeof(Bars) <= 256, "barrier area");
+static_assert(sizeof(Bars) <= 512, "barrier area");
 
 struct Misc {
   uint32_t tmem_base;
   int abort;
   int epi_ok;
+  int epi_task;
+  int task_slot[kTaskSlots];
 };
+static_assert(sizeof(Misc) <= 64, "misc area");
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -156,6 +165,29 @@ __device__ __forceinline__ bool wait_ready(const int* ctr, int target, volatile 
   return true;
 }
 
+// The j-th task of this CTA: the producer posts its id (-1: no more tasks);
+// each of the three readers takes it and frees the slot at once. A reader
+// gets -2 when a wait gave up (the abort flag is set).
+__device__ __forceinline__ bool post_task(Bars* bars, Misc* misc, uint32_t j, int task,
+                                          volatile int* abort) {
+  const int q = static_cast<int>(j % kTaskSlots);
+  const uint32_t round = j / kTaskSlots;
+  if (!ptx::mbar_wait(ptx::smem_u32(&bars->task_empty[q]), (round & 1) ^ 1, abort, kWaitLimitNs))
+    return false;
+  *reinterpret_cast<volatile int*>(&misc->task_slot[q]) = task;
+  ptx::mbar_arrive(ptx::smem_u32(&bars->task_full[q]));
+  return true;
+}
+
+__device__ __forceinline__ int take_task(Bars* bars, Misc* misc, uint32_t j, volatile int* abort) {
+  const int q = static_cast<int>(j % kTaskSlots);
+  const uint32_t round = j / kTaskSlots;
+  if (!ptx::mbar_wait(ptx::smem_u32(&bars->task_full[q]), round & 1, abort, kWaitLimitNs)) return -2;
+  const int task = *reinterpret_cast<volatile int*>(&misc->task_slot[q]);
+  ptx::mbar_arrive(ptx::smem_u32(&bars->task_empty[q]));
+  return task;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_constant__ ExpertParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -176,8 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       ptx::mbar_init(ptx::smem_u32(&bars->tempty[a]), 4);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    for (int q = 0; q < kTaskSlots; ++q) {
+      ptx::mbar_init(ptx::smem_u32(&bars->task_full[q]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->task_empty[q]), 3);
+    }
     misc->abort = 0;
     misc->epi_ok = 0;
+    misc->epi_task = -1;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&p.tm_w13);
     ptx::prefetch_tmap(&p.tm_w13_shared);
@@ -221,10 +258,24 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       // until the previous kernel is done (the first task) and, for a w2 task,
       // until its unit's w13 tiles are done.
       bool waited = false;
-      for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
-        const Task k = decode_task(task, n13, p);
-        const int4 a = __ldcg(act + k.u);
-        if (!task_valid(a, p)) continue;
+      // The next id is fetched as soon as a task starts, so the atomic's
+      // latency hides behind the task's stages.
+      int task = atomicAdd(p.task_ctr, 1), next = 0;
+      for (uint32_t j = 0; ok; ++j, task = next) {
+        Task k = {0, 0, 0};
+        int4 a = make_int4(0, 0, 0, 0);
+        for (; task < ntasks; task = atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
+          k = decode_task(task, n13, p);
+          a = __ldcg(act + k.u);
+          if (task_valid(a, p)) break;
+        }
+        const bool last = task >= ntasks;
+        if (!post_task(bars, misc, j, last ? -1 : task, abort)) {
+          ok = false;
+          break;
+        }
+        if (last) break;
+        next = atomicAdd(p.task_ctr, 1);
         const int nt = (a.z + 15) & ~15;
         const uint32_t pbytes = nt * 128 + kImgBytes;  // the panel's used part
         const uint32_t bytes = kABytes + pbytes;
@@ -300,10 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       uint32_t it = 0;
       int lt = 0;
       bool ok = true;
-      for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
+      for (uint32_t j = 0; ok; ++j) {
+        const int task = take_task(bars, misc, j, abort);
+        if (task < 0) break;
         const Task k = decode_task(task, n13, p);
         const int4 a = __ldcg(act + k.u);
-        if (!task_valid(a, p)) continue;
         const int nt = (a.z + 15) & ~15;
         const int G = k.phase ? p.g2 : p.g13;
         const int acc = lt & 1;
@@ -352,10 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     // slot's 32 x 16-byte image (the stage's 16-byte entry in every row).
     uint32_t it = 0;
     bool ok = true;
-    for (int task = blockIdx.x; task < ntasks && ok; task += gridDim.x) {
+    for (uint32_t j = 0; ok; ++j) {
+      int task = lane == 0 ? take_task(bars, misc, j, abort) : 0;
+      task = __shfl_sync(0xffffffffu, task, 0);
+      if (task < 0) break;
       const Task k = decode_task(task, n13, p);
       const int4 a = __ldcg(act + k.u);
-      if (!task_valid(a, p)) continue;
       const int G = k.phase ? p.g2 : p.g13;
       const uint4* sfa = k.phase ? p.sfa2 + (static_cast<size_t>(a.x) * p.t2 + k.t) * G
                                  : p.sfa13 + (static_cast<size_t>(a.x) * p.t13 + k.t) * G;
@@ -387,10 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [n][64] up values
     ptx::griddep_wait();  // before writing rows the previous kernels may read
     int lt = 0;
-    for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
+    for (uint32_t j = 0;; ++j) {
+      if (threadIdx.x == 128) misc->epi_task = take_task(bars, misc, j, abort);
+      epi_bar();
+      const int task = *reinterpret_cast<volatile int*>(&misc->epi_task);
+      if (task < 0) break;
       const Task k = decode_task(task, n13, p);
       const int4 a = __ldcg(act + k.u);
-      if (!task_valid(a, p)) continue;
       const int rows = a.z;
       const int nt = (rows + 15) & ~15;
       const int acc = lt & 1;

@@ -33,6 +33,7 @@ constexpr int kCtrErr = 0;       // device error word (bit set)
 constexpr int kCtrTicket = 1;    // top-k: token CTAs done
 constexpr int kCtrUnits = 2;     // active experts this step (routed + 1 shared)
 constexpr int kCtrRouted = 3;    // distinct routed experts this step
+constexpr int kCtrTasks = 4;     // expert kernel: next task to hand out (zeroed by the top-k kernel)
 constexpr int kCtrWords = 64;
 
 // One active expert of a step: what the expert kernels need to find its
@@ -133,6 +134,7 @@ struct ExpertParams {
   uint8_t* hpan;              // [units][I/128] panels of h8 rows (written by the w13 epilogue)
   float* part;                // [rows][H]
   int* ready;                 // [E + 1]: finished w13 tiles per unit (zeroed by the top-k kernel)
+  int* task_ctr;              // next task id to hand out (zeroed by the top-k kernel)
   int* err;
   int E;                      // routed experts (index E = shared)
   int inter, hidden;

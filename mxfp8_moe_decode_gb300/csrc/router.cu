@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
       p.counters[kCtrUnits] = iact + 1;
       p.counters[kCtrRouted] = iact;
       p.counters[kCtrTicket] = 0;  // ready for the next step
+      p.counters[kCtrTasks] = 0;   // the expert kernel hands out tasks from zero
     }
   }
   __syncthreads();
