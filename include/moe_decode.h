@@ -62,7 +62,7 @@ extern "C" {
  *  hidden        H: multiple of 128, 256..8192.
  *  experts       E: routed experts, multiple of 32, 32..512.
  *  topk          k: 1..16 and <= E.
- *  inter         I: routed expert intermediate size, multiple of 128, <= 8192.
+ *  inter         I: routed expert intermediate size, multiple of 128, in [256, 8192].
  *  shared_inter  the shared expert's intermediate size; must equal inter.
  *  max_tokens    largest M a step may use, 1..48 (the pages' MAX_TOKENS).
  *  eps           RMSNorm epsilon (1e-6 for the pages' layer).

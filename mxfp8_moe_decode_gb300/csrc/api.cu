@@ -118,7 +118,8 @@ int validate_config(const moe_config* c) {
   if (c->hidden % 128 || c->hidden < 256 || c->hidden > 8192) return MOE_ERR_UNSUPPORTED;
   if (c->experts % 32 || c->experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (c->topk > kMaxTopk || c->topk > c->experts) return MOE_ERR_UNSUPPORTED;
-  if (c->inter % 128 || c->inter > 8192 || c->shared_inter != c->inter) return MOE_ERR_UNSUPPORTED;
+  if (c->inter % 128 || c->inter < 256 || c->inter > 8192 || c->shared_inter != c->inter)
+    return MOE_ERR_UNSUPPORTED;
   if (c->max_tokens > kMaxTokens) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }

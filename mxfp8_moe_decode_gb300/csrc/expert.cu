@@ -34,14 +34,18 @@
 // contiguous bulk copy of the activation panel (rows + scale image, already
 // in the swizzled layout the MMA reads, evict-last). Warp 3 writes each stage's weight-scale image (the
 // stage's 16-byte entry in all 32 rows tcgen05.cp expects) as soon as the
-// slot is free. Warp 1 lane 0 copies both scale images into TMEM and issues 4
-// MMAs (K = 32 each, the descriptor's scale-factor id picks the K block of the
-// stage); warp 2 owns the TMEM allocation; warps 4-7 drain the double-buffered
-// accumulator (each reads its 32-lane quarter). At ~80 cycles per TMA or
-// tcgen05 instruction, the issue cost per 16 KB stage sets the per-SM
-// bandwidth, hence the few instructions per stage. Every mbarrier and
-// readiness wait is bounded; on a timeout the CTA records kErrTimeout, waits
-// for its own copies and MMAs, frees TMEM and exits.
+// slot is free. Two MMA issuers share the stages of every task: lane 0 of
+// warp 1 takes the even K stages, lane 0 of warp 2 (which also owns the TMEM
+// allocation) the odd ones; each copies its stage's two scale images into TMEM
+// and issues 4 MMAs (K = 32 each, the descriptor's scale-factor id picks the K
+// block of the stage) into its own accumulator, and the epilogue adds the two
+// partial sums. One thread needs ~530 cycles to issue a stage (about 100 per
+// MMA, 55 per scale copy); that is more than the ~720 cycles per 16 KB stage
+// at which one SM's share of HBM arrives, minus the slot's other costs, while
+// two issuers work concurrently at the same per-thread rate. Warps 4-7 drain
+// the double-buffered accumulators (each reads its 32-lane quarter). Every
+// mbarrier and readiness wait is bounded; on a timeout the CTA records
+// kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
 //
 // Launched with programmatic dependent launch: the prologue and the first
 // task's weight stages run while the previous kernel finishes; activation
@@ -65,9 +69,10 @@ constexpr uint32_t kOffBar = kOffXchg + kMaxTokens * 64 * 4;
 constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
-constexpr uint32_t kTmemCols = 256;  // 2 accumulators x 64 + 8 stages x 8 scale columns
+// TMEM: 2 task buffers x 2 issuers x 64 accumulator columns, then 8 scale columns per stage
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 64;
-constexpr uint32_t kSfCol0 = 128;
+constexpr uint32_t kSfCol0 = 4 * kAccCols;
 constexpr int kTaskSlots = 8;  // task-id queue from the producer to the other roles
 
 static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "B tiles must stay 1024-aligned");
@@ -84,7 +89,7 @@ struct Bars {
   uint64_t tempty[2];
   uint64_t drain;
   uint64_t task_full[kTaskSlots];   // the producer posted a task id
-  uint64_t task_empty[kTaskSlots];  // the MMA issuer, the helper warp and the epilogue read it
+  uint64_t task_empty[kTaskSlots];  // both MMA issuers, the helper warp and the epilogue read it
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
 
@@ -166,7 +171,7 @@ __device__ __forceinline__ bool wait_ready(const int* ctr, int target, volatile 
 }
 
 // The j-th task of this CTA: the producer posts its id (-1: no more tasks);
-// each of the three readers takes it and frees the slot at once. A reader
+// each of the four readers takes it and frees the slot at once. A reader
 // gets -2 when a wait gave up (the abort flag is set).
 __device__ __forceinline__ bool post_task(Bars* bars, Misc* misc, uint32_t j, int task,
                                           volatile int* abort) {
@@ -204,13 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       ptx::mbar_init(ptx::smem_u32(&bars->sfa_rdy[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(ptx::smem_u32(&bars->tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->tempty[a]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->tfull[a]), 2);   // one commit per issuer
+      ptx::mbar_init(ptx::smem_u32(&bars->tempty[a]), 4);  // one arrival per epilogue warp
     }
-    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), 2);
     for (int q = 0; q < kTaskSlots; ++q) {
       ptx::mbar_init(ptx::smem_u32(&bars->task_full[q]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->task_empty[q]), 3);
+      ptx::mbar_init(ptx::smem_u32(&bars->task_empty[q]), 4);
     }
     misc->abort = 0;
     misc->epi_ok = 0;
@@ -345,8 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // issuer h takes the stages g with g % 2 == h of every task
+    const int h = warp - 1;
     if (lane == 0) {
       uint32_t it = 0;
       int lt = 0;
@@ -366,8 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tbase + acc * kAccCols;
+        const uint32_t d_tmem = tbase + (2 * acc + h) * kAccCols;
         for (int g = 0; g < G; ++g, ++it) {
+          if ((g & 1) != h) continue;
           const int s = it % kStages;
           const uint32_t round = it / kStages;
           if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[s]), round & 1, abort, kWaitLimitNs) ||
@@ -386,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           for (int kk = 0; kk < 4; ++kk) {
             ptx::tc_mma_mxf8(d_tmem, ptx::sdesc_k128_sw128(sa + 32 * kk),
                              ptx::sdesc_k128_sw128(sb + 32 * kk), ptx::idesc_mxf8_e4m3(nt, kk), sf_a,
-                             sf_b, (g | kk) != 0);
+                             sf_b, (g > h) || kk != 0);
           }
           ptx::tc_commit(ptx::smem_u32(&bars->empty[s]));
         }
@@ -460,11 +468,21 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       ptx::mbar_wait(tfull, use & 1, abort, kWaitLimitNs);  // completed: returns at once
       ptx::tc_fence_after();
       float v[kMaxTokens];
-      const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * q) << 16) + acc * kAccCols;
+      float w[kMaxTokens];  // the odd-stage issuer's partial sums
+      const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * q) << 16) + 2 * acc * kAccCols;
       ptx::tmem_ld_32x32b_x16(taddr, v);
-      if (nt > 16) ptx::tmem_ld_32x32b_x16(taddr + 16, v + 16);
-      if (nt > 32) ptx::tmem_ld_32x32b_x16(taddr + 32, v + 32);
+      ptx::tmem_ld_32x32b_x16(taddr + kAccCols, w);
+      if (nt > 16) {
+        ptx::tmem_ld_32x32b_x16(taddr + 16, v + 16);
+        ptx::tmem_ld_32x32b_x16(taddr + kAccCols + 16, w + 16);
+      }
+      if (nt > 32) {
+        ptx::tmem_ld_32x32b_x16(taddr + 32, v + 32);
+        ptx::tmem_ld_32x32b_x16(taddr + kAccCols + 32, w + 32);
+      }
       ptx::tmem_wait_ld();
+#pragma unroll
+      for (int n = 0; n < kMaxTokens; ++n) v[n] += w[n];
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->tempty[acc]));
