@@ -250,9 +250,8 @@ void moe_destroy(moe_handle* h);
  *
  * The first call on a device (with that device current) looks up the array's
  * device address and sets the kernel's shared-memory limit; make that first
- * call before any stream capture. Each call enqueues memsets of the array's
- * counters and expert masks and two kernels on `stream` (void* holding a
- * cudaStream_t). All
+ * call before any stream capture. Each call enqueues a memset of the array's
+ * counters and two kernels on `stream` (void* holding a cudaStream_t). All
  * calls share the one array, which keeps the last call's contents: calls whose
  * work overlaps on the GPU (different streams, or concurrent host threads
  * without ordering) race on it and must be serialised by the caller.

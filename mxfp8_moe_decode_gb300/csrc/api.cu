@@ -32,7 +32,6 @@ struct moe_handle {
   uint8_t* x8;
   uint8_t* x8c;
   float* logit_part;
-  unsigned long long* mask;
   int* ids;
   uint8_t* xpan;
   uint8_t* hpan;
@@ -241,7 +240,6 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   const size_t o_x8 = place(static_cast<size_t>(Mx) * H);
   const size_t o_x8c = place(static_cast<size_t>(Mx) * H / 32);
   const size_t o_lp = place(static_cast<size_t>(ks) * Mx * E * 4);
-  const size_t o_mk = place(static_cast<size_t>(E) * 8);
   const size_t o_id = place(static_cast<size_t>(Mx) * K * 4);
   const size_t o_xp = place(static_cast<size_t>(h->units_max) * g13 * kPanelPitch);
   const size_t o_hp = place(static_cast<size_t>(h->units_max) * g2 * kPanelPitch);
@@ -268,7 +266,6 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->x8 = b + o_x8;
   h->x8c = b + o_x8c;
   h->logit_part = reinterpret_cast<float*>(b + o_lp);
-  h->mask = reinterpret_cast<unsigned long long*>(b + o_mk);
   h->ids = reinterpret_cast<int*>(b + o_id);
   h->xpan = b + o_xp;
   h->hpan = b + o_hp;
@@ -390,7 +387,6 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   tp.bias = h->w.bias;
   tp.counters = h->counters;
   tp.ready = h->ready;
-  tp.mask = h->mask;
   tp.ids = h->ids;
   tp.act = h->act;
   tp.route_w = h->route_w;

@@ -26,7 +26,7 @@ constexpr int kThreads = 256;
 constexpr int kMaxRows = kMaxTokens * (kMaxTopk + 1);
 static_assert(kMaxTokens <= 64, "scale images use cells 0 and 1 only");
 
-__global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p) {
+__global__ void __launch_bounds__(kThreads, 1) gather_kernel(const GatherParams p) {
   // gathered row -> (unit << 16) | (row within the unit << 8) | the unit's padded rows
   __shared__ uint32_t row_map[kMaxRows];
   constexpr uint32_t kNone = 0xffffffffu;
@@ -128,8 +128,11 @@ __global__ void __launch_bounds__(kThreads) sfa_pack_kernel(const SfaPackParams 
 
 }  // namespace
 
+// One CTA per SM: its registers (256 threads x ~32) fit beside the expert
+// kernel's CTA, which then starts (and streams its first weight stages) while
+// the gather still runs.
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s) {
-  return launch_pdl(gather_kernel, dim3(2 * num_sms), dim3(kThreads), 0, s, p);
+  return launch_pdl(gather_kernel, dim3(num_sms), dim3(kThreads), 0, s, p);
 }
 
 cudaError_t launch_sfa_pack(const SfaPackParams& p, cudaStream_t s) {

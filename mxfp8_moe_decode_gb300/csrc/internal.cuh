@@ -71,7 +71,6 @@ struct TopkParams {
   const float* bias;
   int* counters;
   int* ready;                 // [E + 1] expert-kernel readiness counters to clear (or null)
-  unsigned long long* mask;   // [E]: bit m set if token m picked the expert (zero between steps)
   int* ids;                   // [M][k]
   ActiveExpert* act;          // [E + 1]
   float* route_w;             // [M][k]

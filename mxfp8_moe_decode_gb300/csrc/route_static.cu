@@ -83,8 +83,7 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   const size_t o_rw = o_act + align256(static_cast<size_t>(experts + 1) * sizeof(ActiveExpert));
   const size_t o_tp = o_rw + align256(static_cast<size_t>(M) * topk * 4);
   const size_t o_pt = o_tp + align256(static_cast<size_t>(M) * (topk + 1) * 4);
-  const size_t o_mk = o_pt + align256(static_cast<size_t>(M) * (topk + 1) * 4);
-  const size_t o_id = o_mk + align256(static_cast<size_t>(experts) * 8);
+  const size_t o_id = o_pt + align256(static_cast<size_t>(M) * (topk + 1) * 4);
   const size_t o_lp = o_id + align256(static_cast<size_t>(M) * topk * 4);
   const size_t need = o_lp + align256(static_cast<size_t>(ks) * M * experts * 4);
   if (need > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;
@@ -100,10 +99,9 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   uint8_t* base = static_cast<uint8_t*>(base_v);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // the top-k ticket, the error word and the expert masks must start at zero;
-  // the array keeps whatever the previous call left
-  if (cudaMemsetAsync(base + o_ctr, 0, kCtrWords * 4, st) != cudaSuccess ||
-      cudaMemsetAsync(base + o_mk, 0, static_cast<size_t>(experts) * 8, st) != cudaSuccess) {
+  // the top-k ticket and the error word must start at zero; the array keeps
+  // whatever the previous call left
+  if (cudaMemsetAsync(base + o_ctr, 0, kCtrWords * 4, st) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
@@ -121,7 +119,6 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   tp.bias = bias;
   tp.counters = reinterpret_cast<int*>(base + o_ctr);
   tp.ready = nullptr;
-  tp.mask = reinterpret_cast<unsigned long long*>(base + o_mk);
   tp.ids = reinterpret_cast<int*>(base + o_id);
   tp.act = reinterpret_cast<ActiveExpert*>(base + o_act);
   tp.route_w = reinterpret_cast<float*>(base + o_rw);

@@ -11,20 +11,24 @@
 // router_kernel: grid (E / 8, KS) x 256 threads. CTA (b, ks) holds the gate
 // rows of experts 8b .. 8b+7 restricted to the K-slice [ks Hs, (ks + 1) Hs)
 // (loaded before the grid-dependency wait: they do not depend on the seam) and
-// bulk-copies the normed rows' K-slice into shared memory; warp w reduces
-// expert 8b + w over it for every token at once (each lane keeps one fp32 sum
-// per token over its 8-column slices), then one butterfly reduce-scatter
-// across the warp's lanes yields logit_part[ks][m][e].
+// bulk-copies the normed rows' K-slice into shared memory. The product is a
+// small dense contraction, done on the tensor cores with warp-level bf16 MMAs
+// (m16n8k16, fp32 accumulate): tokens are the MMA's rows (16 per tile, up to
+// 3 tiles), the CTA's 8 experts its columns; warp w takes the K-slice's
+// 16-column steps w, w + 8, ...; the 8 warps' partial tiles are then summed
+// in a fixed order into logit_part[ks][m][e]. Row pitches in shared memory are
+// padded by 16 bytes so the fragment loads hit 32 distinct banks.
 //
 // topk_kernel: one CTA per token. A thread per expert sums the KS partial
 // logits in a fixed order (all partial loads issued before the sum), takes
 // sigmoid and score + bias; warp 0 picks the k largest choices with 64-bit
 // keys (order-preserving bits of the choice, then the inverted expert index,
-// so equal choices go to the lower index), one warp-wide max per pick, and
-// sets the token's bit in each picked expert's mask. The last token CTA (a
-// device-scope ticket) compacts: active experts in increasing id each get a
-// contiguous run of gathered rows (tokens in increasing index), the shared
-// expert last with all M tokens; it clears the masks and the ticket.
+// so equal choices go to the lower index), one warp-wide max per pick; lane j
+// keeps pick j. The last token CTA (a device-scope ticket; a single token CTA
+// needs none) compacts: it rebuilds each expert's token mask from all picks in
+// shared memory, then one block-wide scan gives the active experts in
+// increasing id each a contiguous run of gathered rows (tokens in increasing
+// index), the shared expert last with all M tokens; it clears the ticket.
 #include <cfloat>
 #include <cmath>
 
@@ -36,36 +40,28 @@ namespace {
 
 constexpr int kThreads = kRouterWarps * 32;
 constexpr int kMaxHs = 1536;                    // K-slice columns per router CTA
-constexpr int kMaxChunks = kMaxHs / 256;        // 256-column chunks (8 per lane)
+constexpr int kMaxChunks = kMaxHs / 256;        // 256-column chunks (8 columns per lane)
 constexpr int kMaxPerLane = kMaxExperts / 32;
-constexpr int kSlots = 64;                      // token sums per lane (>= kMaxTokens)
 constexpr int kMaxKsplit = 16;                  // K-slices of the router GEMV
 constexpr int kTopkThreads = 256;
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
-  f[0] = __uint_as_float(u.x << 16);
-  f[1] = __uint_as_float(u.x & 0xffff0000u);
-  f[2] = __uint_as_float(u.y << 16);
-  f[3] = __uint_as_float(u.y & 0xffff0000u);
-  f[4] = __uint_as_float(u.z << 16);
-  f[5] = __uint_as_float(u.z & 0xffff0000u);
-  f[6] = __uint_as_float(u.w << 16);
-  f[7] = __uint_as_float(u.w & 0xffff0000u);
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
 }
 
-// One step of the butterfly reduce-scatter: lanes whose `off` bit is clear keep
-// the lower half of the N live slots, the others the upper half; each adds the
-// partner's copy of the half it keeps.
-template <int N>
-__device__ __forceinline__ void reduce_scatter_step(float* v, int off, int lane) {
-  const bool hi = (lane & off) != 0;
-#pragma unroll
-  for (int i = 0; i < N / 2; ++i) {
-    const float send = hi ? v[i] : v[i + N / 2];
-    const float keep = hi ? v[i + N / 2] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-  }
+// D (16 x 8, f32) += A (16 x 16, bf16, row-major) . B (16 x 8, bf16, column-major)
+__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+
+constexpr int kMTiles = (kMaxTokens + 15) / 16;
+
+__host__ __device__ constexpr int router_pitch(int Hs) { return Hs * 2 + 16; }
 
 __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -73,14 +69,19 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
   const int M = p.M, H = p.H, E = p.E, Hs = p.Hs;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = blockIdx.y * Hs;
-  const int oct = Hs >> 3;  // 16-byte pieces of one row slice
-  const uint4* xs = reinterpret_cast<const uint4*>(smem);                      // [M][oct]
-  uint4* gs = reinterpret_cast<uint4*>(smem) + static_cast<size_t>(M) * oct;  // [8][oct]
-  const int e = blockIdx.x * kRouterWarps + warp;
+  const int e0 = blockIdx.x * kRouterWarps;
+  const int mtiles = (M + 15) >> 4;
+  const int ld = router_pitch(Hs);  // bytes per row in shared memory
+  const int rows = 16 * mtiles;
+  uint8_t* xs = smem;                                        // [rows][ld] normed rows
+  uint8_t* gs = smem + static_cast<size_t>(rows) * ld;       // [8][ld] gate rows
+  float* red = reinterpret_cast<float*>(gs + static_cast<size_t>(kRouterWarps) * ld);  // [8][rows][8]
 
   // ---- gate rows first: they do not depend on the previous kernel
   {
-    const uint4* src = reinterpret_cast<const uint4*>(p.gate_w + static_cast<size_t>(e) * H + k0);
+    const int oct = Hs >> 3;  // 16-byte pieces of one row slice
+    const uint4* src =
+        reinterpret_cast<const uint4*>(p.gate_w + static_cast<size_t>(e0 + warp) * H + k0);
     uint4 g[kMaxChunks];
 #pragma unroll
     for (int c = 0; c < kMaxChunks; ++c) {
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
 #pragma unroll
     for (int c = 0; c < kMaxChunks; ++c) {
       const int i = c * 32 + lane;
-      if (i < oct) gs[warp * oct + i] = g[c];
+      if (i < oct) *reinterpret_cast<uint4*>(gs + warp * ld + 16 * i) = g[c];
     }
   }
   if (tid == 0) {
@@ -102,60 +103,58 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
   __syncthreads();
 
   // ---- the K-slice of every normed row: one bulk copy per row, all in flight
+  // (rows M .. rows - 1 are left as they are: they only feed output rows that
+  // are dropped)
   if (tid == 0) {
     const uint32_t b = ptx::smem_u32(&bar);
     ptx::mbar_arrive_expect_tx(b, static_cast<uint32_t>(M) * Hs * 2);
     for (int m = 0; m < M; ++m)
-      ptx::bulk_load(ptx::smem_u32(smem + static_cast<size_t>(m) * Hs * 2),
+      ptx::bulk_load(ptx::smem_u32(xs + static_cast<size_t>(m) * ld),
                      p.normed + static_cast<size_t>(m) * H + k0, Hs * 2, b);
   }
   int never = 0;
   ptx::mbar_wait(ptx::smem_u32(&bar), 0, &never, kWaitLimitNs);
 
-  // ---- every token's sum over this lane's 8-column slices
-  float acc[kSlots];
+  // ---- tensor-core partial products over this warp's 16-column steps
+  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group, column pair
+  float d[kMTiles][4];
 #pragma unroll
-  for (int m = 0; m < kSlots; ++m) acc[m] = 0.0f;
-#pragma unroll 1
-  for (int c = 0; c < kMaxChunks; ++c) {
-    const int i = c * 32 + lane;
-    if (i < oct) {
-      float gf[8];
-      unpack_bf16x8(gs[warp * oct + i], gf);
+  for (int mt = 0; mt < kMTiles; ++mt)
 #pragma unroll
-      for (int m = 0; m < kMaxTokens; ++m) {
-        if (m < M) {
-          float xf[8];
-          unpack_bf16x8(xs[m * oct + i], xf);
+    for (int i = 0; i < 4; ++i) d[mt][i] = 0.0f;
+  const uint8_t* brow = gs + gq * ld + 4 * tq;  // B column gq = gate row e0 + gq
+  for (int st = warp; st < (Hs >> 4); st += kRouterWarps) {
+    const int kb = st * 32;  // byte offset of the step's 16 columns
+    const uint32_t b0 = lds32(brow + kb), b1 = lds32(brow + kb + 16);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[m] = fmaf(gf[j], xf[j], acc[m]);
-        }
+    for (int mt = 0; mt < kMTiles; ++mt) {
+      if (mt < mtiles) {
+        const uint8_t* r0 = xs + (16 * mt + gq) * ld + kb + 4 * tq;
+        const uint8_t* r1 = r0 + 8 * ld;
+        mma_bf16_16816(d[mt], lds32(r0), lds32(r1), lds32(r0 + 16), lds32(r1 + 16), b0, b1);
       }
     }
   }
 
-  // ---- across the warp: a few tokens directly, many by reduce-scatter
-  float* out = p.logit_part + static_cast<size_t>(blockIdx.y) * M * E + e;
-  if (M <= 4) {
+  // ---- the 8 warps' tiles summed in a fixed order
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      if (m < M) {
-        float v = acc[m];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) out[static_cast<size_t>(m) * E] = v;
-      }
+  for (int mt = 0; mt < kMTiles; ++mt) {
+    if (mt < mtiles) {
+      float* t = red + (static_cast<size_t>(warp) * rows + 16 * mt + gq) * 8 + 2 * tq;
+      t[0] = d[mt][0];
+      t[1] = d[mt][1];
+      t[64] = d[mt][2];  // row + 8
+      t[65] = d[mt][3];
     }
-  } else {
-    reduce_scatter_step<64>(acc, 16, lane);
-    reduce_scatter_step<32>(acc, 8, lane);
-    reduce_scatter_step<16>(acc, 4, lane);
-    reduce_scatter_step<8>(acc, 2, lane);
-    reduce_scatter_step<4>(acc, 1, lane);
-    const int m0 = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 +
-                   ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
-    if (m0 < M) out[static_cast<size_t>(m0) * E] = acc[0];
-    if (m0 + 1 < M) out[static_cast<size_t>(m0 + 1) * E] = acc[1];
+  }
+  __syncthreads();
+  float* out = p.logit_part + static_cast<size_t>(blockIdx.y) * M * E + e0;
+  for (int i = tid; i < M * kRouterWarps; i += kThreads) {
+    const int m = i >> 3, c = i & 7;
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kRouterWarps; ++w) v += red[(static_cast<size_t>(w) * rows + m) * 8 + c];
+    out[static_cast<size_t>(m) * E + c] = v;
   }
 }
 
@@ -179,6 +178,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   // ---- one thread per expert: the KS partials (all loads in flight), then
   // their sum in a fixed order, the score and the choice key
   for (int ex = tid; ex < E; ex += kTopkThreads) {
+    const float b = p.bias[ex];
     float part[kMaxKsplit];
 #pragma unroll
     for (int ks = 0; ks < kMaxKsplit; ++ks)
@@ -189,12 +189,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
       if (ks < KS) logit += part[ks];
     const float s = 1.0f / (1.0f + expf(-logit));
     s_s[ex] = s;
-    key_s[ex] = choice_key(s + p.bias[ex], ex);
+    key_s[ex] = choice_key(s + b, ex);
     if (p.dbg_logits) p.dbg_logits[static_cast<size_t>(m) * E + ex] = logit;
   }
   __syncthreads();
 
-  // ---- warp 0: the k largest keys, one warp-wide max per pick
+  // ---- warp 0: the k largest keys, one warp-wide max per pick; lane j keeps
+  // pick j
   if (warp == 0) {
     unsigned long long key[kMaxPerLane];
 #pragma unroll
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     for (int i = 0; i < kMaxPerLane; ++i) best = key[i] > best ? key[i] : best;
     float ssum = 0.0f, my_s = 0.0f;
     int my_id = 0;
+    bool bad = false;
     for (int j = 0; j < K; ++j) {
       unsigned long long w = best;
 #pragma unroll
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
       }
       int ex = 0x7fffffff - static_cast<int>(static_cast<uint32_t>(w));
       if (w == 0ull || ex < 0 || ex >= E) {  // only with non-finite scores
-        if (lane == 0) atomicOr(&p.counters[kCtrErr], kErrBounds);
+        bad = true;
         ex = 0;
       }
       if (lane == (ex & 31)) {
@@ -231,8 +233,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
         my_s = s;
         my_id = ex;
       }
-      if (lane == 0) atomicOr(p.mask + ex, 1ull << m);
     }
+    if (bad && lane == 0) atomicOr(&p.counters[kCtrErr], kErrBounds);
     if (lane < K) {
       const float wgt = my_s / ssum;
       p.route_w[m * K + lane] = wgt;
@@ -240,79 +242,86 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
       if (p.dbg_w) p.dbg_w[m * K + lane] = wgt;
       if (p.dbg_ids) p.dbg_ids[m * K + lane] = my_id;
     }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) is_last = (atomicAdd(&p.counters[kCtrTicket], 1) == M - 1);
+    if (M > 1) {
+      // the last token CTA to get here builds the tables
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) is_last = (atomicAdd(&p.counters[kCtrTicket], 1) == M - 1);
+    } else if (lane == 0) {
+      is_last = 1;
+    }
   }
   __syncthreads();
   if (!is_last) return;
-  __threadfence();
+  if (M > 1) __threadfence();
 
-  // ---- the last token CTA: every mask and pick into shared memory at once
+  // ---- the last token CTA: every pick into shared memory, the per-expert
+  // token masks rebuilt there
   __shared__ int base_s[kMaxExperts];
   __shared__ unsigned long long mask_s[kMaxExperts];
   __shared__ int ids_s[kMaxTokens * kMaxTopk];
-  for (int ex = tid; ex < E; ex += kTopkThreads) {
-    mask_s[ex] = __ldcg(p.mask + ex);
-    p.mask[ex] = 0ull;  // ready for the next step
-  }
+  __shared__ uint32_t wsum_s[kTopkThreads / 32];
+  for (int ex = tid; ex < E; ex += kTopkThreads) mask_s[ex] = 0ull;
   for (int i = tid; i < M * K; i += kTopkThreads) ids_s[i] = __ldcg(p.ids + i);
   if (p.ready)  // the expert kernel's per-unit readiness counts start at zero
     for (int u = tid; u <= E; u += kTopkThreads) p.ready[u] = 0;
   __syncthreads();
+  for (int i = tid; i < M * K; i += kTopkThreads) {
+    const int ex = ids_s[i];
+    if (ex >= 0 && ex < E) atomicOr(&mask_s[ex], 1ull << (i / K));
+  }
+  __syncthreads();
 
-  // ---- warp 0: active experts in increasing id, their row runs
-  if (warp == 0) {
-    const int per = E / 32;
-    int cnt = 0, act = 0;
-    for (int i = 0; i < per; ++i) {
-      const int n = __popcll(mask_s[lane * per + i]);
-      cnt += n;
-      act += n > 0;
-    }
-    int icnt = cnt, iact = act;
+  // ---- active experts in increasing id and their row runs: thread t owns
+  // experts 2t and 2t + 1; one block-wide exclusive scan of (rows << 16 | active)
+  static_assert(kMaxExperts <= 2 * kTopkThreads, "two experts per thread");
+  static_assert(kMaxTokens * kMaxTopk < (1 << 16), "row count fits 16 bits");
+  const int e0 = 2 * tid, e1 = 2 * tid + 1;
+  const int n0 = e0 < E ? __popcll(mask_s[e0]) : 0;
+  const int n1 = e1 < E ? __popcll(mask_s[e1]) : 0;
+  const uint32_t mine = (static_cast<uint32_t>(n0 + n1) << 16) | ((n0 > 0) + (n1 > 0));
+  uint32_t incl = mine;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, icnt, off);
-      const int b = __shfl_up_sync(0xffffffffu, iact, off);
-      if (lane >= off) {
-        icnt += a;
-        iact += b;
-      }
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) wsum_s[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kTopkThreads / 32; ++w) {
+    const uint32_t v = wsum_s[w];
+    before += w < warp ? v : 0u;
+    total += v;
+  }
+  const uint32_t excl = before + incl - mine;
+  int pos = static_cast<int>(excl >> 16), u = static_cast<int>(excl & 0xffffu);
+  if (e0 < E) {
+    base_s[e0] = pos;
+    if (n0 > 0) {
+      p.act[u] = ActiveExpert{e0, pos, n0, 0};
+      ++u;
+      pos += n0;
     }
-    int pos = icnt - cnt, u = iact - act;
-    for (int i = 0; i < per; ++i) {
-      const int ex = lane * per + i;
-      const int n = __popcll(mask_s[ex]);
-      base_s[ex] = pos;
-      if (n > 0) {
-        ActiveExpert a;
-        a.expert = ex;
-        a.pos_base = pos;
-        a.rows = n;
-        a.pad = 0;
-        p.act[u] = a;
-        ++u;
-        pos += n;
-      }
-    }
-    if (lane == 31) {
-      ActiveExpert a;
-      a.expert = E;
-      a.pos_base = icnt;  // == M * K
-      a.rows = M;
-      a.pad = 0;
-      p.act[iact] = a;
-      p.counters[kCtrUnits] = iact + 1;
-      p.counters[kCtrRouted] = iact;
-      p.counters[kCtrTicket] = 0;  // ready for the next step
-      p.counters[kCtrTasks] = 0;   // the expert kernel hands out tasks from zero
-    }
+  }
+  if (e1 < E) {
+    base_s[e1] = pos;
+    if (n1 > 0) p.act[u] = ActiveExpert{e1, pos, n1, 0};
+  }
+  if (tid == 0) {
+    const int routed = static_cast<int>(total & 0xffffu);
+    p.act[routed] = ActiveExpert{E, static_cast<int>(total >> 16), M, 0};  // shared: rows M K..
+    p.counters[kCtrUnits] = routed + 1;
+    p.counters[kCtrRouted] = routed;
+    p.counters[kCtrTicket] = 0;  // ready for the next step
+    p.counters[kCtrTasks] = 0;   // the expert kernel hands out tasks from zero
   }
   __syncthreads();
   for (int i = tid; i < M * K; i += kTopkThreads) {
     const int mm = i / K, j = i - mm * K;
     const int ex = ids_s[i];
+    if (ex < 0 || ex >= E) continue;
     const int rank = __popcll(mask_s[ex] & ((1ull << mm) - 1ull));
     const int pp = base_s[ex] + rank;
     p.tok_pos[mm * (K + 1) + j] = pp;
@@ -333,12 +342,14 @@ int router_ksplit(int hidden, int experts) {
   if (ks < 1) ks = 1;
   if (ks > 16) ks = 16;
   while (hidden / ks > kMaxHs) ks *= 2;
-  while (hidden % (ks * 8)) ks /= 2;
+  while (ks > 1 && hidden % (ks * 16)) ks /= 2;  // whole 16-column MMA steps
   return ks;
 }
 
 size_t router_smem_bytes(int M, int Hs) {
-  return static_cast<size_t>(M + kRouterWarps) * Hs * 2;  // normed slice + gate slice
+  const size_t rows = 16 * static_cast<size_t>((M + 15) / 16);
+  // normed rows (padded to whole MMA tiles) + gate rows + the warps' partial tiles
+  return (rows + kRouterWarps) * router_pitch(Hs) + kRouterWarps * rows * 8 * sizeof(float);
 }
 
 cudaError_t router_setup() {

@@ -37,6 +37,13 @@ __global__ void __launch_bounds__(kThreads) seam_kernel(const SeamParams p) {
   const int tid = threadIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * H);
   const uint4* wr = reinterpret_cast<const uint4*>(p.norm_w);
+  // the norm weight does not depend on earlier work: fetch it before waiting
+  uint4 wraw[kMaxOct];
+#pragma unroll
+  for (int i = 0; i < kMaxOct; ++i) {
+    const int o = tid + i * kThreads;
+    wraw[i] = o < noct ? wr[o] : make_uint4(0, 0, 0, 0);
+  }
   // x comes from the previous kernel on the stream; the router may start now
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
@@ -71,12 +78,7 @@ __global__ void __launch_bounds__(kThreads) seam_kernel(const SeamParams p) {
     if (i * kThreads >= noct) break;  // uniform across the CTA
     const bool live = o < noct;
     float w[8];
-    if (live) {
-      unpack_bf16x8(wr[o], w);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = 0.0f;
-    }
+    unpack_bf16x8(wraw[i], w);  // zero past the row
     float n[8];
     __align__(16) __nv_bfloat16 nb[8];
     float amax = 0.0f;
