@@ -468,21 +468,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       ptx::mbar_wait(tfull, use & 1, abort, kWaitLimitNs);  // completed: returns at once
       ptx::tc_fence_after();
       float v[kMaxTokens];
-      float w[kMaxTokens];  // the odd-stage issuer's partial sums
+      // the even-stage issuer's sums, then the odd-stage issuer's added 16
+      // columns at a time (one 16-register buffer)
       const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * q) << 16) + 2 * acc * kAccCols;
       ptx::tmem_ld_32x32b_x16(taddr, v);
-      ptx::tmem_ld_32x32b_x16(taddr + kAccCols, w);
-      if (nt > 16) {
-        ptx::tmem_ld_32x32b_x16(taddr + 16, v + 16);
-        ptx::tmem_ld_32x32b_x16(taddr + kAccCols + 16, w + 16);
-      }
-      if (nt > 32) {
-        ptx::tmem_ld_32x32b_x16(taddr + 32, v + 32);
-        ptx::tmem_ld_32x32b_x16(taddr + kAccCols + 32, w + 32);
-      }
-      ptx::tmem_wait_ld();
+      if (nt > 16) ptx::tmem_ld_32x32b_x16(taddr + 16, v + 16);
+      if (nt > 32) ptx::tmem_ld_32x32b_x16(taddr + 32, v + 32);
 #pragma unroll
-      for (int n = 0; n < kMaxTokens; ++n) v[n] += w[n];
+      for (int c = 0; c < kMaxTokens / 16; ++c) {
+        if (16 * c < nt) {
+          float w[16];
+          ptx::tmem_ld_32x32b_x16(taddr + kAccCols + 16 * c, w);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int n = 0; n < 16; ++n) v[16 * c + n] += w[n];
+        }
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->tempty[acc]));

@@ -5,10 +5,12 @@
 // the expert's MXFP8 token rows (the order the router chose) as the 128-byte
 // swizzled image the MMA reads, then the stage's scale image -- row r holds in
 // 32-bit cell j the four E8M0 codes (4 consecutive 32-column blocks) of the
-// expert's token 32 j + r, zero past its token count. That image is the layout
-// the block-scaled MMA reads from TMEM (row n of the operand at TMEM lane
-// n % 32, column n / 32; byte b of a cell = K block b of the stage), copied
-// there by tcgen05.cp.
+// expert's token 32 j + r. That image is the layout the block-scaled MMA reads
+// from TMEM (row n of the operand at TMEM lane n % 32, column n / 32; byte b of
+// a cell = K block b of the stage), copied there by tcgen05.cp. Cells of
+// absent tokens are left as they are: they only scale output columns that are
+// dropped. One warp per gathered row: every lane issues all its loads of the
+// token's row and codes, then scatters them into the unit's panels.
 //
 // sfa_pack_kernel (once, at handle creation): the weights' 32 x 32-block E8M0
 // codes ("vllm.models.deepseek_v41.amd.mono.runner", MonoLayerWeights.check:
@@ -22,23 +24,24 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;        // sfa_pack_kernel
+constexpr int kGatherThreads = 128;  // gather_kernel: 4 warps, <= 80 registers each
 constexpr int kMaxRows = kMaxTokens * (kMaxTopk + 1);
 static_assert(kMaxTokens <= 64, "scale images use cells 0 and 1 only");
 
-__global__ void __launch_bounds__(kThreads, 1) gather_kernel(const GatherParams p) {
+__global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(const GatherParams p) {
   // gathered row -> (unit << 16) | (row within the unit << 8) | the unit's padded rows
   __shared__ uint32_t row_map[kMaxRows];
   constexpr uint32_t kNone = 0xffffffffu;
   const int H = p.H, G = p.G;
   const int rows = min(p.M * (p.K + 1), min(p.rows_max, kMaxRows));
-  for (int i = threadIdx.x; i < rows; i += kThreads) row_map[i] = kNone;
+  for (int i = threadIdx.x; i < rows; i += kGatherThreads) row_map[i] = kNone;
   ptx::griddep_wait();  // routing tables and x8 come from the previous kernels
   ptx::griddep_launch_dependents();
   int units = p.counters[kCtrUnits];
   if (units < 0 || units > p.units_max) units = 0;  // the expert kernel reports it
   __syncthreads();
-  for (int u = threadIdx.x; u < units; u += kThreads) {
+  for (int u = threadIdx.x; u < units; u += kGatherThreads) {
     const int4 a = *reinterpret_cast<const int4*>(p.act + u);  // expert, first row, rows, pad
     if (a.y < 0 || a.z < 1 || a.z > kMaxTokens || a.y + a.z > rows) continue;
     const uint32_t nt = static_cast<uint32_t>((a.z + 15) & ~15);
@@ -47,43 +50,50 @@ __global__ void __launch_bounds__(kThreads, 1) gather_kernel(const GatherParams 
   }
   __syncthreads();
 
-  // token rows: one 16-byte chunk per thread and step
+  // one warp per gathered row
+  constexpr int kWarps = kGatherThreads / 32;
+  constexpr int kPassChunks = 10;  // 16-byte chunks per lane and pass (one pass for H <= 5120)
+  constexpr int kMaxStageLanes = 8192 / 128 / 32;  // K stages per lane
+  const int lane = threadIdx.x & 31;
   const int n16 = H >> 4;
-  const long long stride = static_cast<long long>(gridDim.x) * kThreads;
-  const long long start = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
-  for (long long i = start; i < static_cast<long long>(rows) * n16; i += stride) {
-    const int row = static_cast<int>(i / n16);
-    const int c = static_cast<int>(i - static_cast<long long>(row) * n16);
+  const int cstride = H >> 5;  // codes per token row
+  for (int row = blockIdx.x * kWarps + (threadIdx.x >> 5); row < rows; row += gridDim.x * kWarps) {
     const uint32_t map = row_map[row];
     const int m = p.pos_tok[row];
     if (map == kNone || m < 0 || m >= p.M) continue;
     const int u = static_cast<int>(map >> 16), r = static_cast<int>((map >> 8) & 255u);
-    uint8_t* panel = p.xpan + (static_cast<size_t>(u) * G + (c >> 3)) * kPanelPitch;
-    *reinterpret_cast<uint4*>(panel + panel_byte(r, (c & 7) << 4)) =
-        reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H)[c];
-  }
-
-  // scale images: one 16-byte image row per thread and step
-  const int cstride = H >> 5;  // codes per token row
-  for (long long i = start; i < static_cast<long long>(units) * G * 32; i += stride) {
-    const int r = static_cast<int>(i & 31);
-    const long long ug = i >> 5;
-    const int g = static_cast<int>(ug % G);
-    const int u = static_cast<int>(ug / G);
-    const int4 a = *reinterpret_cast<const int4*>(p.act + u);
-    if (a.y < 0 || a.z < 1 || a.z > kMaxTokens || a.y + a.z > rows) continue;
-    const int nt = (a.z + 15) & ~15;
-    uint32_t cell[2] = {0u, 0u};
+    const int nt = static_cast<int>(map & 255u);
+    const uint4* src = reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H);
+    const uint8_t* csrc = p.x8c + static_cast<size_t>(m) * cstride;
+    uint32_t code[kMaxStageLanes];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (32 * j + r < a.z) {
-        const int m = p.pos_tok[a.y + 32 * j + r];
-        if (m >= 0 && m < p.M)
-          cell[j] = *reinterpret_cast<const uint32_t*>(p.x8c + static_cast<size_t>(m) * cstride + 4 * g);
+    for (int j = 0; j < kMaxStageLanes; ++j) {
+      const int g = lane + 32 * j;
+      if (g < G) code[j] = *reinterpret_cast<const uint32_t*>(csrc + 4 * g);
+    }
+    uint8_t* base = p.xpan + static_cast<size_t>(u) * G * kPanelPitch;
+    for (int c0 = 0; c0 < n16; c0 += 32 * kPassChunks) {
+      uint4 v[kPassChunks];
+#pragma unroll
+      for (int i = 0; i < kPassChunks; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < n16) v[i] = src[c];
+      }
+#pragma unroll
+      for (int i = 0; i < kPassChunks; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < n16)
+          *reinterpret_cast<uint4*>(base + (c >> 3) * kPanelPitch + panel_byte(r, (c & 7) << 4)) =
+              v[i];
       }
     }
-    uint8_t* panel = p.xpan + (static_cast<size_t>(u) * G + g) * kPanelPitch;
-    *reinterpret_cast<uint4*>(panel + nt * 128 + r * 16) = make_uint4(cell[0], cell[1], 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < kMaxStageLanes; ++j) {
+      const int g = lane + 32 * j;
+      if (g < G)
+        *reinterpret_cast<uint32_t*>(base + g * kPanelPitch + nt * 128 + (r & 31) * 16 + (r >> 5) * 4) =
+            code[j];
+    }
   }
 }
 
@@ -128,11 +138,11 @@ __global__ void __launch_bounds__(kThreads) sfa_pack_kernel(const SfaPackParams 
 
 }  // namespace
 
-// One CTA per SM: its registers (256 threads x ~32) fit beside the expert
-// kernel's CTA, which then starts (and streams its first weight stages) while
-// the gather still runs.
+// One CTA of 128 threads per SM: its registers fit beside the expert kernel's
+// CTA, which then starts (and streams its first weight stages) while the
+// gather still runs.
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s) {
-  return launch_pdl(gather_kernel, dim3(num_sms), dim3(kThreads), 0, s, p);
+  return launch_pdl(gather_kernel, dim3(num_sms), dim3(kGatherThreads), 0, s, p);
 }
 
 cudaError_t launch_sfa_pack(const SfaPackParams& p, cudaStream_t s) {
