@@ -41,7 +41,6 @@ namespace {
 constexpr int kThreads = kRouterWarps * 32;
 constexpr int kMaxHs = 1536;                    // K-slice columns per router CTA
 constexpr int kMaxChunks = kMaxHs / 256;        // 256-column chunks (8 columns per lane)
-constexpr int kMaxPerLane = kMaxExperts / 32;
 constexpr int kMaxKsplit = 16;                  // K-slices of the router GEMV
 constexpr int kTopkThreads = 256;
 
@@ -167,76 +166,91 @@ __device__ __forceinline__ unsigned long long choice_key(float c, int idx) {
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) {
-  ptx::griddep_wait();  // partial logits come from the router kernel
-  ptx::griddep_launch_dependents();
   const int M = p.M, E = p.E, K = p.K, KS = p.KS;
   const int m = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ unsigned long long key_s[kMaxExperts];
+  __shared__ unsigned long long cand_s[kMaxExperts];  // (E / 32) groups x K
   __shared__ float s_s[kMaxExperts];
+  __shared__ int pick_s[kMaxTopk];
   __shared__ int is_last;
+  static_assert(kMaxExperts <= 2 * kTopkThreads, "two experts per thread");
+  // the bias does not depend on the router: fetch it before waiting
+  float bias[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int ex = tid + i * kTopkThreads;
+    bias[i] = ex < E ? p.bias[ex] : 0.0f;
+  }
+  ptx::griddep_wait();  // partial logits come from the router kernel
+  ptx::griddep_launch_dependents();
 
   // ---- one thread per expert: the KS partials (all loads in flight), then
   // their sum in a fixed order, the score and the choice key
-  for (int ex = tid; ex < E; ex += kTopkThreads) {
-    const float b = p.bias[ex];
-    float part[kMaxKsplit];
 #pragma unroll
-    for (int ks = 0; ks < kMaxKsplit; ++ks)
-      part[ks] = ks < KS ? __ldcg(p.logit_part + (static_cast<size_t>(ks) * M + m) * E + ex) : 0.0f;
-    float logit = 0.0f;
+  for (int i = 0; i < 2; ++i) {
+    const int ex = tid + i * kTopkThreads;
+    if (ex < E) {
+      float part[kMaxKsplit];
 #pragma unroll
-    for (int ks = 0; ks < kMaxKsplit; ++ks)
-      if (ks < KS) logit += part[ks];
-    const float s = 1.0f / (1.0f + expf(-logit));
-    s_s[ex] = s;
-    key_s[ex] = choice_key(s + b, ex);
-    if (p.dbg_logits) p.dbg_logits[static_cast<size_t>(m) * E + ex] = logit;
+      for (int ks = 0; ks < kMaxKsplit; ++ks)
+        part[ks] = ks < KS ? __ldcg(p.logit_part + (static_cast<size_t>(ks) * M + m) * E + ex) : 0.0f;
+      float logit = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < kMaxKsplit; ++ks)
+        if (ks < KS) logit += part[ks];
+      const float s = 1.0f / (1.0f + expf(-logit));
+      s_s[ex] = s;
+      key_s[ex] = choice_key(s + bias[i], ex);
+      if (p.dbg_logits) p.dbg_logits[static_cast<size_t>(m) * E + ex] = logit;
+    }
   }
   __syncthreads();
 
-  // ---- warp 0: the k largest keys, one warp-wide max per pick; lane j keeps
-  // pick j
+  // ---- the k largest keys by rank (keys are distinct: they hold the expert
+  // index): first each expert's rank within its group of 32 (a group's k best
+  // are candidates), then each candidate's rank among all candidates; the
+  // candidate of rank j is pick j
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int ex = tid + i * kTopkThreads;
+    if (ex < E) {
+      const unsigned long long mine = key_s[ex];
+      const unsigned long long* grp = key_s + (ex & ~31);
+      int rank = 0;
+#pragma unroll 8
+      for (int o = 0; o < 32; ++o) rank += grp[o] > mine;
+      if (rank < K) cand_s[(ex >> 5) * K + rank] = mine;
+    }
+  }
+  __syncthreads();
+  const int ncand = (E >> 5) * K;
+  for (int c = tid; c < ncand; c += kTopkThreads) {
+    const unsigned long long mine = cand_s[c];
+    int rank = 0;
+    for (int o = 0; o < ncand; ++o) rank += cand_s[o] > mine;
+    if (rank < K) {
+      const int ex = 0x7fffffff - static_cast<int>(static_cast<uint32_t>(mine));
+      pick_s[rank] = ex;
+    }
+  }
+  __syncthreads();
   if (warp == 0) {
-    unsigned long long key[kMaxPerLane];
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) key[i] = lane + 32 * i < E ? key_s[lane + 32 * i] : 0ull;
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) best = key[i] > best ? key[i] : best;
-    float ssum = 0.0f, my_s = 0.0f;
-    int my_id = 0;
+    // the chosen scores' sum in pick order (the same in every lane)
+    float ssum = 0.0f;
     bool bad = false;
     for (int j = 0; j < K; ++j) {
-      unsigned long long w = best;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, w, off);
-        w = o > w ? o : w;
-      }
-      int ex = 0x7fffffff - static_cast<int>(static_cast<uint32_t>(w));
-      if (w == 0ull || ex < 0 || ex >= E) {  // only with non-finite scores
+      int ex = pick_s[j];
+      if (ex < 0 || ex >= E) {  // only with non-finite scores
         bad = true;
         ex = 0;
       }
-      if (lane == (ex & 31)) {
-        const int slot = ex >> 5;
-        best = 0ull;
-#pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
-          if (i == slot) key[i] = 0ull;
-          best = key[i] > best ? key[i] : best;
-        }
-      }
-      const float s = s_s[ex];
-      ssum += s;
-      if (lane == j) {
-        my_s = s;
-        my_id = ex;
-      }
+      ssum += s_s[ex];
     }
     if (bad && lane == 0) atomicOr(&p.counters[kCtrErr], kErrBounds);
     if (lane < K) {
-      const float wgt = my_s / ssum;
+      int my_id = pick_s[lane];
+      if (my_id < 0 || my_id >= E) my_id = 0;
+      const float wgt = s_s[my_id] / ssum;
       p.route_w[m * K + lane] = wgt;
       p.ids[m * K + lane] = my_id;
       if (p.dbg_w) p.dbg_w[m * K + lane] = wgt;
@@ -262,7 +276,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   __shared__ int ids_s[kMaxTokens * kMaxTopk];
   __shared__ uint32_t wsum_s[kTopkThreads / 32];
   for (int ex = tid; ex < E; ex += kTopkThreads) mask_s[ex] = 0ull;
-  for (int i = tid; i < M * K; i += kTopkThreads) ids_s[i] = __ldcg(p.ids + i);
+  if (M > 1) {
+    for (int i = tid; i < M * K; i += kTopkThreads) ids_s[i] = __ldcg(p.ids + i);
+  } else if (tid < K) {
+    const int ex = pick_s[tid];
+    ids_s[tid] = (ex < 0 || ex >= E) ? 0 : ex;
+  }
   if (p.ready)  // the expert kernel's per-unit readiness counts start at zero
     for (int u = tid; u <= E; u += kTopkThreads) p.ready[u] = 0;
   __syncthreads();
