@@ -98,6 +98,7 @@ struct Misc {
   int abort;
   int epi_ok;
   int epi_task;
+  int ready_seq;  // the last task (sequence number) whose unit's w13 tiles are all done
   int task_slot[kTaskSlots];
 };
 static_assert(sizeof(Misc) <= 64, "misc area");
@@ -193,6 +194,29 @@ __device__ __forceinline__ int take_task(Bars* bars, Misc* misc, uint32_t j, vol
   return task;
 }
 
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(ptx::smem_u32(p)) : "memory");
+  return v;
+}
+
+// Bounded wait until the helper warp has published task j as ready.
+__device__ __forceinline__ bool wait_seq(const int* seq, int j, volatile int* abort) {
+  if (ld_acquire_cta(seq) >= j) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(32);
+    if (ld_acquire_cta(seq) >= j) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_constant__ ExpertParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -220,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     misc->abort = 0;
     misc->epi_ok = 0;
     misc->epi_task = -1;
+    misc->ready_seq = -1;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&p.tm_w13);
     ptx::prefetch_tmap(&p.tm_w13_shared);
@@ -261,15 +286,19 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       // Weight stages never depend on earlier work: they are issued at once.
       // A task's activation stages are held back (at most one ring's worth)
       // until the previous kernel is done (the first task) and, for a w2 task,
-      // until its unit's w13 tiles are done.
+      // until its unit's w13 tiles are done -- which the helper warp finds out
+      // (a device-scope wait here would also wait for this thread's copies in
+      // flight) and publishes in shared memory; they go out as soon as it has.
       bool waited = false;
-      // The next id is fetched as soon as a task starts, so the atomic's
-      // latency hides behind the task's stages.
-      int task = atomicAdd(p.task_ctr, 1), next = 0;
+      // The first task is the CTA's index; later ones come from the counter
+      // (offset by the grid), fetched as soon as a task starts so that the
+      // atomic's latency hides behind the task's stages.
+      const int grid = static_cast<int>(gridDim.x);
+      int task = static_cast<int>(blockIdx.x), next = 0;
       for (uint32_t j = 0; ok; ++j, task = next) {
         Task k = {0, 0, 0};
         int4 a = make_int4(0, 0, 0, 0);
-        for (; task < ntasks; task = atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
+        for (; task < ntasks; task = grid + atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
           k = decode_task(task, n13, p);
           a = __ldcg(act + k.u);
           if (task_valid(a, p)) break;
@@ -280,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           break;
         }
         if (last) break;
-        next = atomicAdd(p.task_ctr, 1);
+        next = grid + atomicAdd(p.task_ctr, 1);
         const int nt = (a.z + 15) & ~15;
         const uint32_t pbytes = nt * 128 + kImgBytes;  // the panel's used part
         const uint32_t bytes = kABytes + pbytes;
@@ -318,18 +347,23 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           } else {
             if (n_pending == 0) first_pending = it;
             ++n_pending;
-            if (n_pending == kStages || g == G - 1) {
-              if (!waited) {
+            bool go = k.phase == 1 && ld_acquire_cta(&misc->ready_seq) >= static_cast<int>(j);
+            if (!go && (n_pending == kStages || g == G - 1)) {
+              if (k.phase == 0 && !waited) {
                 ptx::griddep_wait();
                 waited = true;
               }
               // on a timeout the held-back loads still go out (their data is
               // not used), so that every issued stage completes before exit
-              if (k.phase == 1 && !wait_ready(p.ready + k.u, p.t13, abort)) ok = false;
+              if (k.phase == 1 && !wait_seq(&misc->ready_seq, static_cast<int>(j), abort)) ok = false;
+              go = true;
+            }
+            if (go) {
+              if (k.phase == 1) asm volatile("fence.proxy.async.global;" ::: "memory");
               b_ok = true;
               const int g0 = g - (n_pending - 1);
-              for (int j = 0; j < n_pending; ++j)
-                issue_b(g0 + j, static_cast<int>((first_pending + j) % kStages));
+              for (int q = 0; q < n_pending; ++q)
+                issue_b(g0 + q, static_cast<int>((first_pending + q) % kStages));
               n_pending = 0;
               if (!ok) {
                 ++it;  // count this stage for the drain below
@@ -421,6 +455,18 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       const int G = k.phase ? p.g2 : p.g13;
       const uint4* sfa = k.phase ? p.sfa2 + (static_cast<size_t>(a.x) * p.t2 + k.t) * G
                                  : p.sfa13 + (static_cast<size_t>(a.x) * p.t13 + k.t) * G;
+      if (k.phase == 1) {
+        // the unit's w13 tiles: a device-scope wait, then the news for the producer
+        int ready = 1;
+        if (lane == 0) {
+          ready = wait_ready(p.ready + k.u, p.t13, abort);
+          if (ready)
+            asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(ptx::smem_u32(&misc->ready_seq)),
+                         "r"(static_cast<int>(j))
+                         : "memory");
+        }
+        if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+      }
       const uint4 zero = make_uint4(0, 0, 0, 0);
       const uint4 e0 = lane < G ? __ldg(sfa + lane) : zero;  // stages lane and lane + 32
       const uint4 e1 = lane + 32 < G ? __ldg(sfa + lane + 32) : zero;
