@@ -3,7 +3,7 @@
 
 Metric: microseconds per MoE decode step, with the achieved HBM GB/s of the
 dominant kernel against the measured copy bandwidth. A step is one pass of the
-whole path (seam, router, top-k, gather, the experts, combine) over one
+whole path (seam, router, top-k with the operand panels, the experts, combine) over one
 batch of M synthetic token rows, replayed from a CUDA graph with every input
 resident in HBM; L2 is flushed (a 512 MB write) before every timed step.
 

@@ -186,21 +186,23 @@ const char* moe_kernel_name(int i);
  * Diagnostics: device address and size of one region of the handle's scratch,
  * valid until moe_destroy; contents are those of the last completed step.
  * Regions (layouts are internal and may change):
- *  MOE_REGION_GATHERED  u8  [units][H / 128][6656] activation panels: panel
- *      (u, g) holds active expert u's MXFP8 token rows over K columns
- *      [128 g, 128 g + 128): row r, column c at byte 128 r + 16 ((c / 16) xor
- *      (r % 8)) + c % 16; then, at byte 128 nt (nt = the unit's rows rounded
- *      up to 16), a 32 x 16-byte scale image whose row r, byte 4 j + b is the
- *      E8M0 code of K block b of the unit's token 32 j + r. Rows r >= the
- *      unit's token count are unspecified.
- *  MOE_REGION_H8        u8  [units][I / 128][6656] the same for the
- *      requantised silu(g) * u rows
- *  MOE_REGION_PARTIAL   f32 [rows][H]  expert output rows y, same order
+ *  MOE_REGION_GATHERED  u8  [E + 1][H / 128][7168] activation panels by
+ *      expert id (E = the shared expert): panel (e, g) holds, for K columns
+ *      [128 g, 128 g + 128), a 32 x 16-byte scale image at byte 0 (row r,
+ *      byte 4 j + b = E8M0 code of K block b of the expert's row 32 j + r),
+ *      then from byte 1024 the expert's MXFP8 token rows: row r, column c at
+ *      byte 1024 + 128 r + 16 ((c / 16) xor (r % 8)) + c % 16. Row r of a
+ *      routed expert is the token that took slot r (any order); rows of the
+ *      shared expert are the tokens in order. Rows >= the expert's token
+ *      count, and experts no token picked, are unspecified.
+ *  MOE_REGION_H8        u8  [units][I / 128][7168] the same layout for the
+ *      requantised silu(g) * u rows, by unit (MOE_REGION_ACTIVE order)
+ *  MOE_REGION_PARTIAL   f32 [rows][H]  expert output rows y
  *  MOE_REGION_ACTIVE    i32 [E + 1][4] active experts: expert, first row, rows, 0
  *  MOE_REGION_TOKPOS    i32 [M][k + 1] row of (token, pick); pick k = shared expert
- * rows = M * (k + 1) for the step's M: the routed picks first (experts in
- * increasing id, tokens in increasing index), then the shared expert's M rows;
- * units = the active experts (MOE_REGION_ACTIVE order), at most
+ * rows = M * (k + 1) for the step's M: each active routed expert (increasing
+ * id) owns a run of rows, its tokens in slot order, then the shared expert's M
+ * rows in token order; units = the active experts, at most
  * min(E, max_tokens * k) + 1.
  */
 #define MOE_REGION_GATHERED 0

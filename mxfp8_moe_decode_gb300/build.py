@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_decode.so")
-SOURCES = ["api.cu", "seam.cu", "router.cu", "gather.cu", "expert.cu", "combine.cu",
+SOURCES = ["api.cu", "seam.cu", "router.cu", "scales.cu", "expert.cu", "combine.cu",
            "route_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -27,7 +27,8 @@ struct moe_handle {
   ActiveExpert* act;
   float* route_w;
   int* tok_pos;
-  int* pos_tok;
+  int* slots;
+  int* cnt;
   __nv_bfloat16* normed;
   uint8_t* x8;
   uint8_t* x8c;
@@ -47,8 +48,8 @@ struct moe_handle {
 
 namespace {
 
-const char* const kKernelNames[] = {"seam", "router", "topk", "gather", "experts", "combine"};
-constexpr int kNumKernels = 6;
+const char* const kKernelNames[] = {"seam", "router", "topk", "experts", "combine"};
+constexpr int kNumKernels = 5;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -166,7 +167,7 @@ int moe_scratch_region(const moe_handle* h, int region, void** ptr, size_t* byte
   switch (region) {
     case MOE_REGION_GATHERED:
       *ptr = h->xpan;
-      *bytes = static_cast<size_t>(h->units_max) * (H / 128) * kPanelPitch;
+      *bytes = static_cast<size_t>(h->cfg.experts + 1) * (H / 128) * kPanelPitch;
       return MOE_OK;
     case MOE_REGION_H8:
       *ptr = h->hpan;
@@ -235,13 +236,14 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   const size_t o_act = place(static_cast<size_t>(E + 1) * sizeof(ActiveExpert));
   const size_t o_rw = place(static_cast<size_t>(Mx) * K * 4);
   const size_t o_tp = place(static_cast<size_t>(Mx) * (K + 1) * 4);
-  const size_t o_pt = place(static_cast<size_t>(h->rows_max) * 4);
+  const size_t o_sl = place(static_cast<size_t>(Mx) * K * 4);
+  const size_t o_cn = place(static_cast<size_t>(E + 1) * 4);
   const size_t o_nm = place(static_cast<size_t>(Mx) * H * 2);
   const size_t o_x8 = place(static_cast<size_t>(Mx) * H);
   const size_t o_x8c = place(static_cast<size_t>(Mx) * H / 32);
   const size_t o_lp = place(static_cast<size_t>(ks) * Mx * E * 4);
   const size_t o_id = place(static_cast<size_t>(Mx) * K * 4);
-  const size_t o_xp = place(static_cast<size_t>(h->units_max) * g13 * kPanelPitch);
+  const size_t o_xp = place(static_cast<size_t>(E + 1) * g13 * kPanelPitch);  // by expert id
   const size_t o_hp = place(static_cast<size_t>(h->units_max) * g2 * kPanelPitch);
   const size_t o_pa = place(static_cast<size_t>(h->rows_max) * H * 4);
   const size_t o_a13 = place(static_cast<size_t>(E + 1) * t13 * g13 * 16);
@@ -261,7 +263,8 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->act = reinterpret_cast<ActiveExpert*>(b + o_act);
   h->route_w = reinterpret_cast<float*>(b + o_rw);
   h->tok_pos = reinterpret_cast<int*>(b + o_tp);
-  h->pos_tok = reinterpret_cast<int*>(b + o_pt);
+  h->slots = reinterpret_cast<int*>(b + o_sl);
+  h->cnt = reinterpret_cast<int*>(b + o_cn);
   h->normed = reinterpret_cast<__nv_bfloat16*>(b + o_nm);
   h->x8 = b + o_x8;
   h->x8c = b + o_x8c;
@@ -387,11 +390,17 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   tp.bias = h->w.bias;
   tp.counters = h->counters;
   tp.ready = h->ready;
+  tp.ready_count = E + 1;
   tp.ids = h->ids;
   tp.act = h->act;
   tp.route_w = h->route_w;
   tp.tok_pos = h->tok_pos;
-  tp.pos_tok = h->pos_tok;
+  tp.slots = h->slots;
+  tp.cnt = h->cnt;
+  tp.x8 = h->x8;
+  tp.x8c = h->x8c;
+  tp.xpan = h->xpan;
+  tp.H = H;
   tp.dbg_ids = d.topk_ids;
   tp.dbg_w = d.topk_w;
   tp.dbg_logits = d.logits;
@@ -399,20 +408,6 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   tp.E = E;
   tp.K = K;
   tp.KS = h->ks;
-
-  GatherParams gp;
-  gp.x8 = h->x8;
-  gp.x8c = h->x8c;
-  gp.counters = h->counters;
-  gp.act = h->act;
-  gp.pos_tok = h->pos_tok;
-  gp.xpan = h->xpan;
-  gp.M = M;
-  gp.H = H;
-  gp.K = K;
-  gp.G = H / 128;
-  gp.units_max = h->units_max;
-  gp.rows_max = h->rows_max;
 
   CombineParams cp;
   cp.part = h->part;
@@ -430,12 +425,10 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   mark(2);
   if (err == cudaSuccess) err = launch_topk(tp, st);
   mark(3);
-  if (err == cudaSuccess) err = launch_gather(gp, h->num_sms, st);
-  mark(4);
   if (err == cudaSuccess) err = launch_experts(h->pe, h->num_sms, st);
-  mark(5);
+  mark(4);
   if (err == cudaSuccess) err = launch_combine(cp, st);
-  mark(6);
+  mark(5);
   return cuda_code(err);
 }
 

@@ -16,41 +16,60 @@ namespace {
 constexpr int kThreads = 128;
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
-  ptx::griddep_wait();  // partial rows come from the w2 kernel
-  ptx::griddep_launch_dependents();
   const int m = blockIdx.y;
   const int H = p.H, K = p.K;
   const int col = (blockIdx.x * kThreads + threadIdx.x) * 8;
+  ptx::griddep_wait();  // the routing tables and the partial rows come from earlier kernels
+  ptx::griddep_launch_dependents();
   if (col >= H) return;
+  // picks 0 .. k-1 weighted, then the shared expert (pick k), in this order;
+  // positions, weights and partial rows of up to 9 picks in flight at once
+  constexpr int kBatch = 9;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < K; ++j) {
-    const int pos = p.tok_pos[m * (K + 1) + j];
-    const float w = p.route_w[m * K + j];
-    const float4* src = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(pos) * H + col);
-    const float4 a = src[0], b = src[1];
-    acc[0] = fmaf(w, a.x, acc[0]);
-    acc[1] = fmaf(w, a.y, acc[1]);
-    acc[2] = fmaf(w, a.z, acc[2]);
-    acc[3] = fmaf(w, a.w, acc[3]);
-    acc[4] = fmaf(w, b.x, acc[4]);
-    acc[5] = fmaf(w, b.y, acc[5]);
-    acc[6] = fmaf(w, b.z, acc[6]);
-    acc[7] = fmaf(w, b.w, acc[7]);
-  }
-  {
-    const int pos = p.tok_pos[m * (K + 1) + K];
-    const float4* src = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(pos) * H + col);
-    const float4 a = src[0], b = src[1];
-    acc[0] += a.x;
-    acc[1] += a.y;
-    acc[2] += a.z;
-    acc[3] += a.w;
-    acc[4] += b.x;
-    acc[5] += b.y;
-    acc[6] += b.z;
-    acc[7] += b.w;
+  for (int j0 = 0; j0 <= K; j0 += kBatch) {
+    int pos[kBatch];
+    float w[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int j = j0 + q;
+      pos[q] = j <= K ? p.tok_pos[m * (K + 1) + j] : 0;
+      w[q] = j < K ? p.route_w[m * K + j] : 1.0f;  // the shared expert's weight is 1
+    }
+    float4 v[kBatch][2];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      if (j0 + q <= K) {
+        const float4* src =
+            reinterpret_cast<const float4*>(p.part + static_cast<size_t>(pos[q]) * H + col);
+        v[q][0] = src[0];
+        v[q][1] = src[1];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int j = j0 + q;
+      if (j < K) {
+        acc[0] = fmaf(w[q], v[q][0].x, acc[0]);
+        acc[1] = fmaf(w[q], v[q][0].y, acc[1]);
+        acc[2] = fmaf(w[q], v[q][0].z, acc[2]);
+        acc[3] = fmaf(w[q], v[q][0].w, acc[3]);
+        acc[4] = fmaf(w[q], v[q][1].x, acc[4]);
+        acc[5] = fmaf(w[q], v[q][1].y, acc[5]);
+        acc[6] = fmaf(w[q], v[q][1].z, acc[6]);
+        acc[7] = fmaf(w[q], v[q][1].w, acc[7]);
+      } else if (j == K) {
+        acc[0] += v[q][0].x;
+        acc[1] += v[q][0].y;
+        acc[2] += v[q][0].z;
+        acc[3] += v[q][0].w;
+        acc[4] += v[q][1].x;
+        acc[5] += v[q][1].y;
+        acc[6] += v[q][1].z;
+        acc[7] += v[q][1].w;
+      }
+    }
   }
   __align__(16) __nv_bfloat162 o[4];
 #pragma unroll

@@ -14,7 +14,7 @@
 //
 //  w13 task = (unit, 64 intermediate columns): A = the 64 gate rows over the
 //    matching 64 up rows of w13 (one 3D TMA box), B = the unit's MXFP8 token
-//    rows (its x panels, written by the gather), K = H. Epilogue: silu(g) * u,
+//    rows (its expert's x panels, written by the top-k kernel), K = H. Epilogue: silu(g) * u,
 //    requantised per token in 32-column groups (the seam's mx_code / E4M3
 //    rule) straight into the unit's h panels (rows and scale images); then
 //    the unit's readiness counter +1.
@@ -47,9 +47,10 @@
 // mbarrier and readiness wait is bounded; on a timeout the CTA records
 // kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
 //
-// Launched with programmatic dependent launch: the prologue and the first
-// task's weight stages run while the previous kernel finishes; activation
-// operands and every global write wait for it (griddepcontrol.wait).
+// Launched with programmatic dependent launch: the prologue (barriers, TMEM,
+// tensor-map prefetch) runs while the top-k kernel finishes; everything else
+// waits for it (griddepcontrol.wait) -- the weights to stream depend on the
+// routing it writes.
 #include "internal.cuh"
 #include "mx.cuh"
 #include "ptx.cuh"
@@ -263,10 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
   // reads anything this grid writes
   ptx::griddep_launch_dependents();
 
-  // The routing tables were written by the top-k kernel, two kernels back: it
-  // has completed before this grid could launch (every kernel of the step
-  // waits for its predecessor before it lets the next one start). Read them
-  // past L1.
+  // the routing tables and the x panels come from the top-k kernel
+  ptx::griddep_wait();
   int units = __ldcg(p.counters + kCtrUnits);
   if (units < 0 || units > p.units_max) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
@@ -283,13 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      // Weight stages never depend on earlier work: they are issued at once.
-      // A task's activation stages are held back (at most one ring's worth)
-      // until the previous kernel is done (the first task) and, for a w2 task,
-      // until its unit's w13 tiles are done -- which the helper warp finds out
-      // (a device-scope wait here would also wait for this thread's copies in
-      // flight) and publishes in shared memory; they go out as soon as it has.
-      bool waited = false;
+      // Weight stages are issued at once. A w2 task's activation stages are
+      // held back (at most one ring's worth) until its unit's w13 tiles are
+      // done -- which the helper warp finds out (a device-scope wait here would
+      // also wait for this thread's copies in flight) and publishes in shared
+      // memory; they go out as soon as it has.
       // The first task is the CTA's index; later ones come from the counter
       // (offset by the grid), fetched as soon as a task starts so that the
       // atomic's latency hides behind the task's stages.
@@ -311,16 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         if (last) break;
         next = grid + atomicAdd(p.task_ctr, 1);
         const int nt = (a.z + 15) & ~15;
-        const uint32_t pbytes = nt * 128 + kImgBytes;  // the panel's used part
+        const uint32_t pbytes = kPanelRows + nt * 128;  // the panel's used part
         const uint32_t bytes = kABytes + pbytes;
         const bool shared_e = a.x == p.E;
         const int G = k.phase ? p.g2 : p.g13;
-        const uint8_t* pan = (k.phase ? p.hpan : p.xpan) + static_cast<size_t>(k.u) * G * kPanelPitch;
+        // x panels are kept per expert id, h panels per unit
+        const uint8_t* pan = k.phase ? p.hpan + static_cast<size_t>(k.u) * G * kPanelPitch
+                                     : p.xpan + static_cast<size_t>(a.x) * G * kPanelPitch;
         auto issue_b = [&](int g, int s) {
           ptx::bulk_load(ptx::smem_u32(smem + kOffB + s * kBBytes), pan + g * kPanelPitch, pbytes,
                          ptx::smem_u32(&bars->full[s]), pol_x);
         };
-        bool b_ok = waited && k.phase == 0;
+        bool b_ok = k.phase == 0;
         int first_pending = 0, n_pending = 0;
         for (int g = 0; g < G; ++g, ++it) {
           const int s = it % kStages;
@@ -349,10 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
             ++n_pending;
             bool go = k.phase == 1 && ld_acquire_cta(&misc->ready_seq) >= static_cast<int>(j);
             if (!go && (n_pending == kStages || g == G - 1)) {
-              if (k.phase == 0 && !waited) {
-                ptx::griddep_wait();
-                waited = true;
-              }
               // on a timeout the held-back loads still go out (their data is
               // not used), so that every issued stage completes before exit
               if (k.phase == 1 && !wait_seq(&misc->ready_seq, static_cast<int>(j), abort)) ok = false;
@@ -373,7 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           }
         }
       }
-      if (!waited) ptx::griddep_wait();
       // wait for every copy still in flight before the CTA may exit
       const uint32_t issued = it;
       for (int s = 0; s < kStages; ++s) {
@@ -421,9 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           const uint32_t sf_a = tbase + kSfCol0 + s * 8;
           const uint32_t sf_b = sf_a + 4;
           const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
-          const uint32_t sb = ptx::smem_u32(smem + kOffB + s * kBBytes);
+          const uint32_t sp = ptx::smem_u32(smem + kOffB + s * kBBytes);  // scale image, then rows
+          const uint32_t sb = sp + kPanelRows;
           ptx::tc_cp_32x128b_x4(sf_a, ptx::sdesc_rows16(ptx::smem_u32(smem + kOffSfa + s * kImgBytes)));
-          ptx::tc_cp_32x128b_x4(sf_b, ptx::sdesc_rows16(sb + nt * 128));
+          ptx::tc_cp_32x128b_x4(sf_b, ptx::sdesc_rows16(sp));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             ptx::tc_mma_mxf8(d_tmem, ptx::sdesc_k128_sw128(sa + 32 * kk),
@@ -493,7 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     // ------------------------------------------------------------ epilogue
     const int q = warp - 4;  // TMEM lane quarter
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [n][64] up values
-    ptx::griddep_wait();  // before writing rows the previous kernels may read
     int lt = 0;
     for (uint32_t j = 0;; ++j) {
       if (threadIdx.x == 128) misc->epi_task = take_task(bars, misc, j, abort);
@@ -551,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           const int i = 64 * k.t + 32 * q + lane;  // intermediate column
           const int kb = i >> 5;                   // its 32-column block
           uint8_t* panel = p.hpan + (static_cast<size_t>(k.u) * p.g2 + (i >> 7)) * kPanelPitch;
-          uint8_t* img = panel + nt * 128 + (kb & 3);
+          uint8_t* img = panel + (kb & 3);
 #pragma unroll
           for (int n = 0; n < kMaxTokens; ++n) {
             if (n < rows) {
@@ -564,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
               const int code = mx_code(amax);
               panel[panel_byte(n, i & 127)] = e4m3(clamp_e4m3(h * mx_mul(code)));
-              if (lane == 0) img[(n & 31) * 16 + (n >> 5) * 4] = static_cast<uint8_t>(code);
+              if (lane == 0) img[panel_code_byte(n)] = static_cast<uint8_t>(code);
             }
           }
           // publish this tile's h8 columns and codes to the w2 tasks (their

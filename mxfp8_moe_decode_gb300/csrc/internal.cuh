@@ -40,7 +40,7 @@ constexpr int kCtrWords = 64;
 // weights and its token rows.
 struct ActiveExpert {
   int expert;    // 0..E-1 routed, E = the shared expert
-  int pos_base;  // first row of its tokens in the gathered activation rows
+  int pos_base;  // first of its partial-output rows
   int rows;      // number of its tokens (1..M)
   int pad;
 };
@@ -66,56 +66,56 @@ struct RouterParams {
   int M, H, E, KS, Hs;
 };
 
+// Activation panels. The B operand of one K stage of one expert is stored as
+// the exact shared-memory image the MMA reads, behind its scale image, so that
+// one contiguous bulk copy stages both:
+//   bytes [0, 512): 32 rows x 16 bytes, row r holding in its 32-bit cell j the
+//     four E8M0 codes of the stage's K blocks for the expert's row 32 j + r;
+//   bytes [512, 1024): unused (the rows start 1024-aligned);
+//   bytes [1024, 1024 + nt * 128): the rows (nt = rows rounded up to 16), 128
+//     bytes of K each, 128-byte swizzled: the 16-byte chunk c of row r sits at
+//     chunk c ^ (r % 8) of that row (the layout a 128B-swizzle TMA box writes).
+// Nothing in a panel depends on the final row count, so rows can be written as
+// soon as their position is known. Panels sit at a fixed pitch. Rows past an
+// expert's token count hold stale finite data: an MMA output column depends on
+// its own row alone and is never read.
+constexpr uint32_t kPanelRows = 1024;
+constexpr uint32_t kPanelPitch = kPanelRows + kMaxTokens * 128;
+static_assert(kPanelPitch % 16 == 0, "bulk copies need 16-byte multiples");
+
+__host__ __device__ __forceinline__ uint32_t panel_byte(int r, int k) {
+  return kPanelRows + static_cast<uint32_t>(r) * 128u +
+         ((static_cast<uint32_t>(k >> 4) ^ (r & 7)) << 4) + static_cast<uint32_t>(k & 15);
+}
+__host__ __device__ __forceinline__ uint32_t panel_code_byte(int r) {
+  return static_cast<uint32_t>(r & 31) * 16u + static_cast<uint32_t>(r >> 5) * 4u;
+}
+
 struct TopkParams {
   const float* logit_part;    // [KS][M][E]
   const float* bias;
   int* counters;
-  int* ready;                 // [E + 1] expert-kernel readiness counters to clear (or null)
+  int* ready;                 // the expert kernel's per-unit readiness counts to clear (or null)
+  int ready_count;            // entries in ready
+  int* cnt;                   // [E + 1]: rows taken per expert this step (zero between steps)
   int* ids;                   // [M][k]
+  int* slots;                 // [M][k]: the token's row among the expert's rows
   ActiveExpert* act;          // [E + 1]
   float* route_w;             // [M][k]
-  int* tok_pos;               // [M][k + 1]: gathered row of (token, pick); pick k = shared
-  int* pos_tok;               // [M (k + 1)]: token of each gathered row
+  int* tok_pos;               // [M][k + 1]: partial-output row of (token, pick); pick k = shared
+  const uint8_t* x8;          // [M][H] the seam's MXFP8 rows and codes [M][H/32]
+  const uint8_t* x8c;
+  uint8_t* xpan;              // [E + 1][H/128] x panels by expert id (or null: no panels)
   int32_t* dbg_ids;
   float* dbg_w;
   float* dbg_logits;
-  int M, E, K, KS;
-};
-
-// Activation panels. The B operand of one K stage of one unit is stored as the
-// exact shared-memory image the MMA reads, followed by its scale image, so that
-// one contiguous bulk copy stages both:
-//   bytes [0, nt * 128): the unit's rows (nt = rows rounded up to 16), 128 bytes
-//     of K each, 128-byte swizzled: the 16-byte chunk c of row r sits at chunk
-//     c ^ (r % 8) of that row (the layout a 128B-swizzle TMA box writes);
-//   bytes [nt * 128, nt * 128 + 512): 32 rows x 16 bytes, row r holding in its
-//     32-bit cell j the four E8M0 codes of the stage's K blocks for token 32 j + r.
-// Panels sit at a fixed pitch: panel (u, g) at ((u * G + g) * kPanelPitch).
-// Rows past a unit's token count hold stale finite data: the MMA output column
-// of such a row depends on that row alone and is never read.
-constexpr uint32_t kPanelPitch = kMaxTokens * 128 + 512;
-static_assert(kPanelPitch % 16 == 0, "bulk copies need 16-byte multiples");
-
-__host__ __device__ __forceinline__ uint32_t panel_byte(int r, int k) {
-  return static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(k >> 4) ^ (r & 7)) << 4) +
-         static_cast<uint32_t>(k & 15);
-}
-
-struct GatherParams {
-  const uint8_t* x8;
-  const uint8_t* x8c;
-  const int* counters;
-  const ActiveExpert* act;
-  const int* pos_tok;
-  uint8_t* xpan;   // [units][H/128] panels of the units' x8 rows
-  int M, H, K, G;  // G = H / 128
-  int units_max, rows_max;
+  int M, E, K, KS, H;
 };
 
 // The grouped-expert kernel's parameters. One launch runs both GEMM phases:
 // first every (unit, w13 tile) task, then every (unit, w2 tile) task.
 //  w13 task = (unit, 64 intermediate columns): A = the 64 gate rows over the
-//    matching 64 up rows, B = the unit's gathered MXFP8 rows, K = H; epilogue:
+//    matching 64 up rows, B = the expert's x panels (MXFP8 token rows), K = H; epilogue:
 //    SwiGLU + requant into h8 rows and the w2 activation-scale images.
 //  w2 task = (unit, 128 hidden rows): A = w2 rows, B = the unit's h8 rows,
 //    K = I; epilogue: fp32 rows of y for the combine. It waits until all
@@ -129,8 +129,8 @@ struct ExpertParams {
   const ActiveExpert* act;
   const uint4* sfa13;         // [E + 1][I/64][H/128] compact weight-scale entries
   const uint4* sfa2;          // [E + 1][H/128][I/128]
-  const uint8_t* xpan;        // [units][H/128] panels of x8 rows (written by the gather)
-  uint8_t* hpan;              // [units][I/128] panels of h8 rows (written by the w13 epilogue)
+  const uint8_t* xpan;        // [E + 1][H/128] x panels by expert id (written by the top-k kernel)
+  uint8_t* hpan;              // [units][I/128] h panels by unit (written by the w13 epilogue)
   float* part;                // [rows][H]
   int* ready;                 // [E + 1]: finished w13 tiles per unit (zeroed by the top-k kernel)
   int* task_ctr;              // next task id to hand out (zeroed by the top-k kernel)
@@ -140,7 +140,7 @@ struct ExpertParams {
   int t13, g13;               // w13: tiles per unit (I/64), K stages (H/128)
   int t2, g2;                 // w2: tiles per unit (H/128), K stages (I/128)
   int units_max;              // capacity of the active-expert table
-  int rows_max;               // capacity of the gathered rows
+  int rows_max;               // capacity of the partial-output rows
 };
 
 struct CombineParams {
@@ -187,7 +187,6 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 cudaError_t router_setup();
 size_t router_smem_bytes(int M, int Hs);
 int router_ksplit(int hidden, int experts);
-cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s);
 cudaError_t expert_kernel_setup();
 size_t expert_smem_bytes(int phase);

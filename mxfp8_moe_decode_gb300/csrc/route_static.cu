@@ -82,8 +82,9 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   const size_t o_act = o_ctr + align256(kCtrWords * 4);
   const size_t o_rw = o_act + align256(static_cast<size_t>(experts + 1) * sizeof(ActiveExpert));
   const size_t o_tp = o_rw + align256(static_cast<size_t>(M) * topk * 4);
-  const size_t o_pt = o_tp + align256(static_cast<size_t>(M) * (topk + 1) * 4);
-  const size_t o_id = o_pt + align256(static_cast<size_t>(M) * (topk + 1) * 4);
+  const size_t o_sl = o_tp + align256(static_cast<size_t>(M) * (topk + 1) * 4);
+  const size_t o_cn = o_sl + align256(static_cast<size_t>(M) * topk * 4);
+  const size_t o_id = o_cn + align256(static_cast<size_t>(experts + 1) * 4);
   const size_t o_lp = o_id + align256(static_cast<size_t>(M) * topk * 4);
   const size_t need = o_lp + align256(static_cast<size_t>(ks) * M * experts * 4);
   if (need > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;
@@ -99,9 +100,10 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   uint8_t* base = static_cast<uint8_t*>(base_v);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // the top-k ticket and the error word must start at zero; the array keeps
-  // whatever the previous call left
-  if (cudaMemsetAsync(base + o_ctr, 0, kCtrWords * 4, st) != cudaSuccess) {
+  // the top-k ticket, the error word and the per-expert row counters must
+  // start at zero; the array keeps whatever the previous call left
+  if (cudaMemsetAsync(base + o_ctr, 0, kCtrWords * 4, st) != cudaSuccess ||
+      cudaMemsetAsync(base + o_cn, 0, static_cast<size_t>(experts + 1) * 4, st) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
@@ -119,11 +121,17 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   tp.bias = bias;
   tp.counters = reinterpret_cast<int*>(base + o_ctr);
   tp.ready = nullptr;
+  tp.ready_count = 0;
   tp.ids = reinterpret_cast<int*>(base + o_id);
   tp.act = reinterpret_cast<ActiveExpert*>(base + o_act);
   tp.route_w = reinterpret_cast<float*>(base + o_rw);
   tp.tok_pos = reinterpret_cast<int*>(base + o_tp);
-  tp.pos_tok = reinterpret_cast<int*>(base + o_pt);
+  tp.slots = reinterpret_cast<int*>(base + o_sl);
+  tp.cnt = reinterpret_cast<int*>(base + o_cn);
+  tp.x8 = nullptr;
+  tp.x8c = nullptr;
+  tp.xpan = nullptr;
+  tp.H = hidden;
   tp.dbg_ids = topk_ids;
   tp.dbg_w = topk_w;
   tp.dbg_logits = nullptr;

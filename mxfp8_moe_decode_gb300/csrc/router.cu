@@ -24,11 +24,15 @@
 // sigmoid and score + bias; warp 0 picks the k largest choices with 64-bit
 // keys (order-preserving bits of the choice, then the inverted expert index,
 // so equal choices go to the lower index), one warp-wide max per pick; lane j
-// keeps pick j. The last token CTA (a device-scope ticket; a single token CTA
-// needs none) compacts: it rebuilds each expert's token mask from all picks in
-// shared memory, then one block-wide scan gives the active experts in
-// increasing id each a contiguous run of gathered rows (tokens in increasing
-// index), the shared expert last with all M tokens; it clears the ticket.
+// keeps pick j and takes the token's row (slot) among the expert's rows with an
+// atomic on a per-expert counter; then the CTA writes the token's MXFP8 row and
+// codes into the x panels of its k experts and of the shared expert (row =
+// token index) -- the panels are the expert kernel's B operand. The last token
+// CTA (a device-scope ticket; a single token CTA needs none) compacts: it
+// counts each expert's rows from all picks in shared memory, then one
+// block-wide scan gives the active experts in increasing id each a contiguous
+// run of partial-output rows, the shared expert last with all M tokens; it
+// clears the counters and the ticket.
 #include <cfloat>
 #include <cmath>
 
@@ -172,6 +176,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   __shared__ unsigned long long cand_s[kMaxExperts];  // (E / 32) groups x K
   __shared__ float s_s[kMaxExperts];
   __shared__ int pick_s[kMaxTopk];
+  __shared__ int slot_s[kMaxTopk];
   __shared__ int is_last;
   static_assert(kMaxExperts <= 2 * kTopkThreads, "two experts per thread");
   // the bias does not depend on the router: fetch it before waiting
@@ -251,11 +256,50 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
       int my_id = pick_s[lane];
       if (my_id < 0 || my_id >= E) my_id = 0;
       const float wgt = s_s[my_id] / ssum;
+      // the token's row among the expert's rows this step (any order: an MMA
+      // output column depends on its own row only)
+      const int slot = atomicAdd(p.cnt + my_id, 1);
       p.route_w[m * K + lane] = wgt;
       p.ids[m * K + lane] = my_id;
+      p.slots[m * K + lane] = slot;
+      pick_s[lane] = my_id;
+      slot_s[lane] = slot;
       if (p.dbg_w) p.dbg_w[m * K + lane] = wgt;
       if (p.dbg_ids) p.dbg_ids[m * K + lane] = my_id;
     }
+  }
+  __syncthreads();
+
+  // ---- this token's MXFP8 row and codes into the x panels of its experts
+  // (row = its slot) and of the shared expert (row = the token index): each
+  // 16-byte piece is read once and stored k + 1 times
+  if (p.xpan) {
+    const int H = p.H, G = H >> 7, n16 = H >> 4;
+    const uint4* xrow = reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H);
+    for (int c = tid; c < n16; c += kTopkThreads) {
+      const uint4 v = xrow[c];
+      for (int d = 0; d <= K; ++d) {
+        const int e = d < K ? pick_s[d] : E;
+        const int r = d < K ? slot_s[d] : m;
+        if (r < 0 || r >= kMaxTokens) continue;
+        *reinterpret_cast<uint4*>(p.xpan + (static_cast<size_t>(e) * G + (c >> 3)) * kPanelPitch +
+                                  panel_byte(r, (c & 7) << 4)) = v;
+      }
+    }
+    const uint8_t* crow = p.x8c + static_cast<size_t>(m) * (H >> 5);
+    for (int g = tid; g < G; g += kTopkThreads) {
+      const uint32_t code = *reinterpret_cast<const uint32_t*>(crow + 4 * g);
+      for (int d = 0; d <= K; ++d) {
+        const int e = d < K ? pick_s[d] : E;
+        const int r = d < K ? slot_s[d] : m;
+        if (r < 0 || r >= kMaxTokens) continue;
+        *reinterpret_cast<uint32_t*>(p.xpan + (static_cast<size_t>(e) * G + g) * kPanelPitch +
+                                     panel_code_byte(r)) = code;
+      }
+    }
+  }
+
+  if (warp == 0) {
     if (M > 1) {
       // the last token CTA to get here builds the tables
       __threadfence();
@@ -269,35 +313,40 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   if (!is_last) return;
   if (M > 1) __threadfence();
 
-  // ---- the last token CTA: every pick into shared memory, the per-expert
-  // token masks rebuilt there
+  // ---- the last token CTA: every pick and slot into shared memory, the
+  // per-expert row counts rebuilt there
   __shared__ int base_s[kMaxExperts];
-  __shared__ unsigned long long mask_s[kMaxExperts];
+  __shared__ int cnt_s[kMaxExperts];
   __shared__ int ids_s[kMaxTokens * kMaxTopk];
+  __shared__ int slots_s[kMaxTokens * kMaxTopk];
   __shared__ uint32_t wsum_s[kTopkThreads / 32];
-  for (int ex = tid; ex < E; ex += kTopkThreads) mask_s[ex] = 0ull;
+  for (int ex = tid; ex < E; ex += kTopkThreads) cnt_s[ex] = 0;
   if (M > 1) {
-    for (int i = tid; i < M * K; i += kTopkThreads) ids_s[i] = __ldcg(p.ids + i);
+    for (int i = tid; i < M * K; i += kTopkThreads) {
+      ids_s[i] = __ldcg(p.ids + i);
+      slots_s[i] = __ldcg(p.slots + i);
+    }
   } else if (tid < K) {
-    const int ex = pick_s[tid];
-    ids_s[tid] = (ex < 0 || ex >= E) ? 0 : ex;
+    ids_s[tid] = pick_s[tid];
+    slots_s[tid] = slot_s[tid];
   }
+  // every token CTA has taken its slots: the per-expert counters start over
+  for (int ex = tid; ex < E; ex += kTopkThreads) p.cnt[ex] = 0;
   if (p.ready)  // the expert kernel's per-unit readiness counts start at zero
-    for (int u = tid; u <= E; u += kTopkThreads) p.ready[u] = 0;
+    for (int i = tid; i < p.ready_count; i += kTopkThreads) p.ready[i] = 0;
   __syncthreads();
   for (int i = tid; i < M * K; i += kTopkThreads) {
     const int ex = ids_s[i];
-    if (ex >= 0 && ex < E) atomicOr(&mask_s[ex], 1ull << (i / K));
+    if (ex >= 0 && ex < E) atomicAdd(&cnt_s[ex], 1);
   }
   __syncthreads();
 
   // ---- active experts in increasing id and their row runs: thread t owns
   // experts 2t and 2t + 1; one block-wide exclusive scan of (rows << 16 | active)
-  static_assert(kMaxExperts <= 2 * kTopkThreads, "two experts per thread");
   static_assert(kMaxTokens * kMaxTopk < (1 << 16), "row count fits 16 bits");
   const int e0 = 2 * tid, e1 = 2 * tid + 1;
-  const int n0 = e0 < E ? __popcll(mask_s[e0]) : 0;
-  const int n1 = e1 < E ? __popcll(mask_s[e1]) : 0;
+  const int n0 = e0 < E ? cnt_s[e0] : 0;
+  const int n1 = e1 < E ? cnt_s[e1] : 0;
   const uint32_t mine = (static_cast<uint32_t>(n0 + n1) << 16) | ((n0 > 0) + (n1 > 0));
   uint32_t incl = mine;
 #pragma unroll
@@ -337,20 +386,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     p.counters[kCtrTasks] = 0;   // the expert kernel hands out tasks from zero
   }
   __syncthreads();
+  // partial-output row of every (token, pick): the expert's run + the slot
   for (int i = tid; i < M * K; i += kTopkThreads) {
     const int mm = i / K, j = i - mm * K;
-    const int ex = ids_s[i];
-    if (ex < 0 || ex >= E) continue;
-    const int rank = __popcll(mask_s[ex] & ((1ull << mm) - 1ull));
-    const int pp = base_s[ex] + rank;
-    p.tok_pos[mm * (K + 1) + j] = pp;
-    p.pos_tok[pp] = mm;
+    const int ex = ids_s[i], sl = slots_s[i];
+    if (ex < 0 || ex >= E || sl < 0 || sl >= cnt_s[ex]) continue;
+    p.tok_pos[mm * (K + 1) + j] = base_s[ex] + sl;
   }
-  for (int mm = tid; mm < M; mm += kTopkThreads) {
-    const int pp = M * K + mm;
-    p.tok_pos[mm * (K + 1) + K] = pp;
-    p.pos_tok[pp] = mm;
-  }
+  for (int mm = tid; mm < M; mm += kTopkThreads) p.tok_pos[mm * (K + 1) + K] = M * K + mm;
 }
 
 }  // namespace

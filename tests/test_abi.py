@@ -37,9 +37,9 @@ def test_exports_every_declared_symbol(L):
 
 def test_kernel_names(L):
     n = L.moe_kernel_count()
-    assert n == 6
+    assert n == 5
     names = [L.moe_kernel_name(i).decode() for i in range(n)]
-    assert names == ["seam", "router", "topk", "gather", "experts", "combine"]
+    assert names == ["seam", "router", "topk", "experts", "combine"]
     assert L.moe_kernel_name(n) is None
 
 
