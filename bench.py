@@ -233,6 +233,20 @@ def time_layer(layer, x, dev, steps: int, warmup: int, flush):
     return step_ms, kmean, unique, g, out
 
 
+def per_step_us(total_ms: float, steps: int, world: int, device=None) -> float:
+    """Whole-job microseconds per step: the slowest rank's timed total (a MAX
+    all-reduce over the process group when world > 1) over the steps all
+    ranks ran (each rank runs an independent replica of the step)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms * 1e3 / (steps * world)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -264,12 +278,7 @@ def run_gpu(args):
         step_ms, kmean, unique, graph, out = time_layer(layer, x, dev, args.steps, args.warmup,
                                                         flush)
     clocks = clk.summary()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    us_step = total_ms * 1e3 / (args.steps * world)
+    us_step = per_step_us(sum(step_ms), args.steps, world, dev)
     names = kernel_names()
     alg = W.algorithmic_bytes(d, unique)
     ix = names.index("experts")

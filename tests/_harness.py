@@ -42,11 +42,14 @@ class Layer:
     """The workload's layer on the GPU plus oracle accessors over the same
     weight tensors (copied to the host one expert at a time)."""
 
-    def __init__(self, wl: W.Workload, device="cuda:0", max_tokens: int | None = None):
+    def __init__(self, wl: W.Workload, device="cuda:0", max_tokens: int | None = None,
+                 bias: torch.Tensor | None = None):
         self.wl = wl
         d = wl.dims
         self.dev = torch.device(device)
         self.ri = W.router_inputs(wl)
+        if bias is not None:  # a routing scenario the workload's bias does not give
+            self.ri["bias"] = bias.to(torch.float32).cpu()
         self.ew = W.expert_weights(wl, device=self.dev)
         weights = {"norm_w": self.ri["norm_w"].to(self.dev), "gate_w": self.ri["gate_w"].to(self.dev),
                    "bias": self.ri["bias"].to(self.dev), **self.ew}

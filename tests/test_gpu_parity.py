@@ -148,3 +148,60 @@ def test_full_size(name, sample):
         L.close()
         del L
         torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- limits and degenerate routing
+
+def test_max_experts_and_topk():
+    # 512 routed experts (two per top-k thread, 16 candidate groups), top-16
+    # (picks beyond one combine batch), 48 tokens
+    wl = W.Workload("limits_e512_k16", W.MoeDims(256, 512, 16, 256, 256), 48, 5, "normal")
+    # at H = 256 the scores of 512 experts crowd together; a bias with 0.05
+    # steps over a seeded permutation spreads the choices so that draws with
+    # every top-17 gap > 1e-3 exist
+    perm = np.random.default_rng([5, 99]).permutation(512)
+    bias = torch.zeros(512, dtype=torch.float32)
+    bias[torch.from_numpy(perm)] = -0.05 * torch.arange(512, dtype=torch.float32)
+    L = Layer(wl, bias=bias)
+    try:
+        x, _ = gapped_tokens(L.wl, L.ri)
+        err, _ = check(L, x, label="E512 k16")
+        print(f"E512 k16 M48: rel err {err:.2e}")
+    finally:
+        L.close()
+
+
+def test_max_hidden_and_inter():
+    # H = I = 8192: 64 K stages per w13 and w2 task, 128 w13 tiles per expert,
+    # the largest seam row; output checked on token 0 (the oracle's expert path
+    # at this size is slow), seam and routing on every token
+    wl = W.Workload("limits_h8192_i8192", W.MoeDims(8192, 32, 2, 8192, 8192), 2, 6, "normal")
+    L = Layer(wl)
+    try:
+        x, _ = gapped_tokens(L.wl, L.ri)
+        err, _ = check(L, x, tokens=[0], label="H8192 I8192")
+        print(f"H8192 I8192: rel err {err:.2e}")
+    finally:
+        L.close()
+
+
+def test_every_token_on_the_same_experts():
+    # a bias that sends all 48 tokens to the same k experts: every routed unit
+    # has 48 rows (MMA N = 48), the other experts are idle
+    wl = W.WORKLOADS["tiny_m1"]
+    d = wl.dims
+    bias = W.router_inputs(wl)["bias"].clone()
+    hot = [5, 17, 33, 60]
+    for j, e in enumerate(hot):
+        bias[e] = 5.0 + 2.0 * j  # steps larger than any score difference
+    L = Layer(wl, bias=bias)
+    try:
+        x, _ = gapped_tokens(L.wl, L.ri, m=48)
+        err, _ = check(L, x, label="same experts")
+        out, dbg = L.run(x)
+        ids = dbg["topk_ids"].numpy()
+        assert np.all(ids == np.array(hot[::-1])[None, :]), ids[:2]
+        assert L.layer.unique_experts() == d.topk
+        print(f"same experts M48: rel err {err:.2e}")
+    finally:
+        L.close()
