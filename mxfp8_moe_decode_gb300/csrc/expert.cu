@@ -17,34 +17,43 @@
 //    rows (its expert's x panels, written by the top-k kernel), K = H. Epilogue: silu(g) * u,
 //    requantised per token in 32-column groups (the seam's mx_code / E4M3
 //    rule) straight into the unit's h panels (rows and scale images); then
-//    the unit's readiness counter +1.
+//    the unit's readiness counter +1 (one device-scope release per tile).
 //  w2 task = (unit, 128 hidden rows): A = w2 rows, B = the unit's h panels,
 //    K = I. Its weight stages are issued at once; its activation stages wait
 //    (bounded) until all w13 tiles of the unit are done. Epilogue: fp32 rows
 //    of y for the combine.
-// Tasks are handed out in that order from a global counter: a CTA's producer
-// takes the next id when it starts a task and passes the ids on to the CTA's
-// other roles through a small queue in shared memory. Every w13 task is handed
-// out before any w2 task, to a CTA that finishes it without waiting on
-// anything, so the readiness waits always end (all CTAs of the grid, one per
-// SM, are resident).
+// Tasks are handed out in that order from a global counter. Every w13 task
+// is handed out before any w2 task, to a CTA that finishes it without waiting
+// on anything, so the readiness waits always end (all CTAs of the grid, one
+// per SM, are resident).
 //
-// Per CTA (one per SM, 256 threads): warp 0 lane 0 issues the loads into an
-// 8-stage ring -- per stage one weight box (TMA, evict-first from L2) and one
-// contiguous bulk copy of the activation panel (rows + scale image, already
-// in the swizzled layout the MMA reads, evict-last). Warp 3 writes each stage's weight-scale image (the
-// stage's 16-byte entry in all 32 rows tcgen05.cp expects) as soon as the
-// slot is free. Two MMA issuers share the stages of every task: lane 0 of
-// warp 1 takes the even K stages, lane 0 of warp 2 (which also owns the TMEM
-// allocation) the odd ones; each copies its stage's two scale images into TMEM
-// and issues 4 MMAs (K = 32 each, the descriptor's scale-factor id picks the K
-// block of the stage) into its own accumulator, and the epilogue adds the two
-// partial sums. One thread needs ~530 cycles to issue a stage (about 100 per
-// MMA, 55 per scale copy); that is more than the ~720 cycles per 16 KB stage
-// at which one SM's share of HBM arrives, minus the slot's other costs, while
-// two issuers work concurrently at the same per-thread rate. Warps 4-7 drain
-// the double-buffered accumulators (each reads its 32-lane quarter). Every
-// mbarrier and readiness wait is bounded; on a timeout the CTA records
+// Per CTA (one per SM, 288 threads):
+//  warp 8 lane 0, the scheduler, claims the CTA's tasks one ahead of the
+//    producer (the next one when the producer has 4 stages of the current one
+//    left to issue, so that a w2 task is rarely claimed long before its unit
+//    can be done), posts each id with its unit's table entry to a small queue
+//    in shared memory, and for a w2 task waits (device scope) for the unit's
+//    readiness and publishes it in shared memory. A device-scope wait in the
+//    producer thread would also wait for its copies in flight.
+//  warp 0 lane 0, the producer, issues the loads into an 8-stage ring -- per
+//    stage one weight box (TMA, evict-first from L2) and one contiguous bulk
+//    copy of the activation panel (rows + scale image, already in the
+//    swizzled layout the MMA reads, evict-last).
+//  warp 3 writes each stage's weight-scale image (the stage's 16-byte entry in
+//    all 32 rows tcgen05.cp expects) as soon as the slot is free.
+//  lane 0 of warps 1 and 2, the MMA issuers, share the stages of every task:
+//    warp 1 takes the even K stages, warp 2 (which also owns the TMEM
+//    allocation) the odd ones; each copies its stage's two scale images into
+//    TMEM and issues 4 MMAs (K = 32 each, the descriptor's scale-factor id
+//    picks the K block of the stage) into its own accumulator, and the
+//    epilogue adds the two partial sums. One thread needs ~530 cycles to
+//    issue a stage (about 100 per MMA, 55 per scale copy); that is more than
+//    the ~720 cycles per 16 KB stage at which one SM's share of HBM arrives,
+//    minus the slot's other costs, while two issuers work concurrently at the
+//    same per-thread rate.
+//  warps 4-7 drain the double-buffered accumulators (each reads its 32-lane
+//    quarter).
+// Every mbarrier and readiness wait is bounded; on a timeout the CTA records
 // kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
 //
 // Launched with programmatic dependent launch: the prologue (barriers, TMEM,
@@ -58,7 +67,7 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;  // 9 warps
 constexpr uint32_t kABytes = kTileM * kStageK;           // 16 KB
 constexpr uint32_t kImgBytes = 32 * 16;                  // scale image of one stage
 constexpr uint32_t kBBytes = 7 * 1024;  // one activation panel (<= 48 rows + image), 1024-aligned
@@ -66,15 +75,20 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffXchg = kOffSfa + kStages * kImgBytes;
-constexpr uint32_t kOffBar = kOffXchg + kMaxTokens * 64 * 4;
+constexpr uint32_t kOffBar = kOffXchg + 2 * kMaxTokens * 64 * 4;  // gate and up values
 constexpr uint32_t kOffMisc = kOffBar + 512;
-constexpr uint32_t kSmemUsed = kOffMisc + 64;
+constexpr uint32_t kSmemUsed = kOffMisc + 256;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 // TMEM: 2 task buffers x 2 issuers x 64 accumulator columns, then 8 scale columns per stage
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 64;
 constexpr uint32_t kSfCol0 = 4 * kAccCols;
-constexpr int kTaskSlots = 8;  // task-id queue from the producer to the other roles
+constexpr int kTaskSlots = 8;  // task-id queue from the scheduler warp to the other roles
+// The producer lets the scheduler claim the next task when this many of the
+// current task's stages are left to issue (the ring holds 8 more): late enough
+// that a w2 task is rarely claimed before its unit can be done, early enough
+// that the claim, its table read and the readiness check are over in time.
+constexpr int kClaimLead = 4;
 
 static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "B tiles must stay 1024-aligned");
 static_assert(kBBytes >= kPanelPitch, "a panel fits its slot");
@@ -95,14 +109,17 @@ struct Bars {
 static_assert(sizeof(Bars) <= 512, "barrier area");
 
 struct Misc {
+  int4 slot_act[kTaskSlots];  // the posted task's unit entry (expert id, first row, rows)
+  int4 epi_act;
   uint32_t tmem_base;
   int abort;
   int epi_ok;
   int epi_task;
   int ready_seq;  // the last task (sequence number) whose unit's w13 tiles are all done
+  int prod_seq;   // the last task (sequence number) the producer has taken
   int task_slot[kTaskSlots];
 };
-static_assert(sizeof(Misc) <= 64, "misc area");
+static_assert(sizeof(Misc) <= 256, "misc area");
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -172,27 +189,40 @@ __device__ __forceinline__ bool wait_ready(const int* ctr, int target, volatile 
   return true;
 }
 
-// The j-th task of this CTA: the producer posts its id (-1: no more tasks);
-// each of the four readers takes it and frees the slot at once. A reader
-// gets -2 when a wait gave up (the abort flag is set).
-__device__ __forceinline__ bool post_task(Bars* bars, Misc* misc, uint32_t j, int task,
+// The j-th task of this CTA: the scheduler posts its id (-1: no more tasks)
+// with its unit's table entry; each of the five readers takes both and frees
+// the slot at once. A reader gets -2 when a wait gave up (the abort flag is set).
+constexpr int kTaskReaders = 5;  // producer, two MMA issuers, scale-image warp, epilogue
+__device__ __forceinline__ bool post_task(Bars* bars, Misc* misc, uint32_t j, int task, int4 a,
                                           volatile int* abort) {
   const int q = static_cast<int>(j % kTaskSlots);
   const uint32_t round = j / kTaskSlots;
   if (!ptx::mbar_wait(ptx::smem_u32(&bars->task_empty[q]), (round & 1) ^ 1, abort, kWaitLimitNs))
     return false;
   *reinterpret_cast<volatile int*>(&misc->task_slot[q]) = task;
+  volatile int4* dst = &misc->slot_act[q];
+  dst->x = a.x;
+  dst->y = a.y;
+  dst->z = a.z;
+  dst->w = a.w;
   ptx::mbar_arrive(ptx::smem_u32(&bars->task_full[q]));
   return true;
 }
 
-__device__ __forceinline__ int take_task(Bars* bars, Misc* misc, uint32_t j, volatile int* abort) {
+__device__ __forceinline__ int take_task(Bars* bars, Misc* misc, uint32_t j, volatile int* abort,
+                                         int4* a) {
   const int q = static_cast<int>(j % kTaskSlots);
   const uint32_t round = j / kTaskSlots;
   if (!ptx::mbar_wait(ptx::smem_u32(&bars->task_full[q]), round & 1, abort, kWaitLimitNs)) return -2;
   const int task = *reinterpret_cast<volatile int*>(&misc->task_slot[q]);
+  const volatile int4* src = &misc->slot_act[q];
+  *a = make_int4(src->x, src->y, src->z, src->w);
   ptx::mbar_arrive(ptx::smem_u32(&bars->task_empty[q]));
   return task;
+}
+
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(ptx::smem_u32(p)), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int ld_acquire_cta(const int* p) {
@@ -240,12 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 2);
     for (int q = 0; q < kTaskSlots; ++q) {
       ptx::mbar_init(ptx::smem_u32(&bars->task_full[q]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->task_empty[q]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->task_empty[q]), kTaskReaders);
     }
     misc->abort = 0;
     misc->epi_ok = 0;
     misc->epi_task = -1;
     misc->ready_seq = -1;
+    misc->prod_seq = -1;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&p.tm_w13);
     ptx::prefetch_tmap(&p.tm_w13_shared);
@@ -284,29 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       bool ok = true;
       // Weight stages are issued at once. A w2 task's activation stages are
       // held back (at most one ring's worth) until its unit's w13 tiles are
-      // done -- which the helper warp finds out (a device-scope wait here would
-      // also wait for this thread's copies in flight) and publishes in shared
-      // memory; they go out as soon as it has.
-      // The first task is the CTA's index; later ones come from the counter
-      // (offset by the grid), fetched as soon as a task starts so that the
-      // atomic's latency hides behind the task's stages.
-      const int grid = static_cast<int>(gridDim.x);
-      int task = static_cast<int>(blockIdx.x), next = 0;
-      for (uint32_t j = 0; ok; ++j, task = next) {
-        Task k = {0, 0, 0};
-        int4 a = make_int4(0, 0, 0, 0);
-        for (; task < ntasks; task = grid + atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
-          k = decode_task(task, n13, p);
-          a = __ldcg(act + k.u);
-          if (task_valid(a, p)) break;
-        }
-        const bool last = task >= ntasks;
-        if (!post_task(bars, misc, j, last ? -1 : task, abort)) {
-          ok = false;
-          break;
-        }
-        if (last) break;
-        next = grid + atomicAdd(p.task_ctr, 1);
+      // done -- which the scheduler warp finds out (a device-scope wait here
+      // would also wait for this thread's copies in flight) and publishes in
+      // shared memory; they go out as soon as it has.
+      for (uint32_t j = 0; ok; ++j) {
+        int4 a;
+        const int task = take_task(bars, misc, j, abort, &a);
+        if (task < 0) break;  // -1: no more tasks; -2: a wait gave up
+        const Task k = decode_task(task, n13, p);
         const int nt = (a.z + 15) & ~15;
         const uint32_t pbytes = kPanelRows + nt * 128;  // the panel's used part
         const uint32_t bytes = kABytes + pbytes;
@@ -321,7 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         };
         bool b_ok = k.phase == 0;
         int first_pending = 0, n_pending = 0;
+        const int claim_g = G > kClaimLead ? G - kClaimLead : 0;
         for (int g = 0; g < G; ++g, ++it) {
+          if (g == claim_g) st_release_cta(&misc->prod_seq, static_cast<int>(j));  // claim the next
           const int s = it % kStages;
           const uint32_t round = it / kStages;
           if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty[s]), (round & 1) ^ 1, abort,
@@ -387,10 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       int lt = 0;
       bool ok = true;
       for (uint32_t j = 0; ok; ++j) {
-        const int task = take_task(bars, misc, j, abort);
+        int4 a;
+        const int task = take_task(bars, misc, j, abort, &a);
         if (task < 0) break;
         const Task k = decode_task(task, n13, p);
-        const int4 a = __ldcg(act + k.u);
         const int nt = (a.z + 15) & ~15;
         const int G = k.phase ? p.g2 : p.g13;
         const int acc = lt & 1;
@@ -442,26 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     uint32_t it = 0;
     bool ok = true;
     for (uint32_t j = 0; ok; ++j) {
-      int task = lane == 0 ? take_task(bars, misc, j, abort) : 0;
+      int4 a = make_int4(0, 0, 0, 0);
+      int task = lane == 0 ? take_task(bars, misc, j, abort, &a) : 0;
       task = __shfl_sync(0xffffffffu, task, 0);
       if (task < 0) break;
+      const int ex = __shfl_sync(0xffffffffu, a.x, 0);  // the unit's expert id
       const Task k = decode_task(task, n13, p);
-      const int4 a = __ldcg(act + k.u);
       const int G = k.phase ? p.g2 : p.g13;
-      const uint4* sfa = k.phase ? p.sfa2 + (static_cast<size_t>(a.x) * p.t2 + k.t) * G
-                                 : p.sfa13 + (static_cast<size_t>(a.x) * p.t13 + k.t) * G;
-      if (k.phase == 1) {
-        // the unit's w13 tiles: a device-scope wait, then the news for the producer
-        int ready = 1;
-        if (lane == 0) {
-          ready = wait_ready(p.ready + k.u, p.t13, abort);
-          if (ready)
-            asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(ptx::smem_u32(&misc->ready_seq)),
-                         "r"(static_cast<int>(j))
-                         : "memory");
-        }
-        if (!__shfl_sync(0xffffffffu, ready, 0)) break;
-      }
+      const uint4* sfa = k.phase ? p.sfa2 + (static_cast<size_t>(ex) * p.t2 + k.t) * G
+                                 : p.sfa13 + (static_cast<size_t>(ex) * p.t13 + k.t) * G;
       const uint4 zero = make_uint4(0, 0, 0, 0);
       const uint4 e0 = lane < G ? __ldg(sfa + lane) : zero;  // stages lane and lane + 32
       const uint4 e1 = lane + 32 < G ? __ldg(sfa + lane + 32) : zero;
@@ -484,18 +491,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->sfa_rdy[s]));
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp - 4;  // TMEM lane quarter
-    float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [n][64] up values
+    float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [gate | up][n][64]
     int lt = 0;
     for (uint32_t j = 0;; ++j) {
-      if (threadIdx.x == 128) misc->epi_task = take_task(bars, misc, j, abort);
+      if (threadIdx.x == 128) {
+        int4 ta;
+        misc->epi_task = take_task(bars, misc, j, abort, &ta);
+        misc->epi_act = ta;
+      }
       epi_bar();
       const int task = *reinterpret_cast<volatile int*>(&misc->epi_task);
       if (task < 0) break;
       const Task k = decode_task(task, n13, p);
-      const int4 a = __ldcg(act + k.u);
+      const int4 a = misc->epi_act;
       const int rows = a.z;
       const int nt = (rows + 15) & ~15;
       const int acc = lt & 1;
@@ -535,44 +546,71 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           if (n < rows) dst[static_cast<size_t>(n) * p.hidden] = v[n];
         epi_bar();
       } else {
-        if (q >= 2) {
+        // gate (warps 4-5) and up (warps 6-7) values to shared memory, then
+        // warp q makes h for the 32 columns 32 (q & 1) .. of rows q >> 1,
+        // (q >> 1) + 2, ... in a short loop
+        const int c = 32 * (q & 1) + lane;  // column within the tile
+        float* gu = xchg + (q >= 2 ? kMaxTokens * 64 : 0);
 #pragma unroll
-          for (int n = 0; n < kMaxTokens; ++n)
-            if (n < rows) xchg[n * 64 + 32 * (q - 2) + lane] = v[n];
-        }
+        for (int n = 0; n < kMaxTokens; ++n)
+          if (n < rows) gu[n * 64 + c] = v[n];
         epi_bar();
-        if (q < 2) {
-          const int i = 64 * k.t + 32 * q + lane;  // intermediate column
-          const int kb = i >> 5;                   // its 32-column block
-          uint8_t* panel = p.hpan + (static_cast<size_t>(k.u) * p.g2 + (i >> 7)) * kPanelPitch;
-          uint8_t* img = panel + (kb & 3);
+        const int i = 64 * k.t + c;  // intermediate column
+        const int kb = i >> 5;       // its 32-column block
+        uint8_t* panel = p.hpan + (static_cast<size_t>(k.u) * p.g2 + (i >> 7)) * kPanelPitch;
+        uint8_t* img = panel + (kb & 3);
+#pragma unroll 1
+        for (int n = q >> 1; n < rows; n += 2) {
+          const float gv = xchg[n * 64 + c];
+          const float uv = xchg[(kMaxTokens + n) * 64 + c];
+          const float h = (gv / (1.0f + expf(-gv))) * uv;
+          float amax = fabsf(h);
 #pragma unroll
-          for (int n = 0; n < kMaxTokens; ++n) {
-            if (n < rows) {
-              const float gv = v[n];
-              const float uv = xchg[n * 64 + 32 * q + lane];
-              const float h = (gv / (1.0f + expf(-gv))) * uv;
-              float amax = fabsf(h);
-#pragma unroll
-              for (int off = 16; off > 0; off >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-              const int code = mx_code(amax);
-              panel[panel_byte(n, i & 127)] = e4m3(clamp_e4m3(h * mx_mul(code)));
-              if (lane == 0) img[panel_code_byte(n)] = static_cast<uint8_t>(code);
-            }
-          }
-          // publish this tile's h8 columns and codes to the w2 tasks (their
-          // bulk copies read them): fence, then the barrier, then one release count
-          __threadfence();
-          asm volatile("fence.proxy.async.global;" ::: "memory");
+          for (int off = 16; off > 0; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+          const int code = mx_code(amax);
+          panel[panel_byte(n, i & 127)] = e4m3(clamp_e4m3(h * mx_mul(code)));
+          if (lane == 0) img[panel_code_byte(n)] = static_cast<uint8_t>(code);
         }
+        // publish the tile's h8 columns and codes to the w2 tasks' bulk
+        // copies: each writer's proxy fence, the barrier, then one release
+        // count (a device-scope release orders the writes the barrier made
+        // visible to the releasing thread; every device-scope fence here
+        // waits for the SM's copies in flight, so there is just one)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
         epi_bar();
-        if (threadIdx.x == 128) {
-          __threadfence();
+        if (threadIdx.x == 128)
           asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.ready + k.u) : "memory");
-        }
       }
     }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ scheduler
+    // Claims the CTA's tasks, one ahead of the producer: the first is the
+    // CTA's index, each later one comes from the counter (offset by the grid)
+    // once the producer has taken the previous one. It posts each with its
+    // unit's entry, then -- for a w2 task -- waits (device scope) until the
+    // unit's w13 tiles are all done and publishes that for the producer, so
+    // the check runs while the producer still streams the previous task.
+    if (lane == 0) {
+      const int grid = static_cast<int>(gridDim.x);
+      int task = static_cast<int>(blockIdx.x);
+      for (uint32_t j = 0;; ++j) {
+        Task k = {0, 0, 0};
+        int4 a = make_int4(0, 0, 0, 0);
+        for (; task < ntasks; task = grid + atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
+          k = decode_task(task, n13, p);
+          a = __ldcg(act + k.u);
+          if (task_valid(a, p)) break;
+        }
+        const bool last = task >= ntasks;
+        if (!post_task(bars, misc, j, last ? -1 : task, a, abort) || last) break;
+        if (k.phase == 1 && !wait_ready(p.ready + k.u, p.t13, abort)) break;
+        st_release_cta(&misc->ready_seq, static_cast<int>(j));
+        if (!wait_seq(&misc->prod_seq, static_cast<int>(j), abort)) break;
+        task = grid + atomicAdd(p.task_ctr, 1);
+      }
+    }
+    __syncwarp();
   }
 
   // ------------------------------------------------------------ teardown

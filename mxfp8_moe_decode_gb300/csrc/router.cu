@@ -47,6 +47,8 @@ constexpr int kMaxHs = 1536;                    // K-slice columns per router CT
 constexpr int kMaxChunks = kMaxHs / 256;        // 256-column chunks (8 columns per lane)
 constexpr int kMaxKsplit = 16;                  // K-slices of the router GEMV
 constexpr int kTopkThreads = 256;
+static_assert(8192 / 16 <= 2 * kTopkThreads && 8192 / 128 <= kTopkThreads,
+              "the top-k kernel holds a token row of up to 8192 columns in registers");
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
@@ -189,6 +191,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   ptx::griddep_wait();  // partial logits come from the router kernel
   ptx::griddep_launch_dependents();
 
+  // this token's MXFP8 row (16-byte pieces) and scale codes (one word per 128
+  // columns), loaded now so that their latency hides behind the selection;
+  // they are stored into the picked experts' panels below
+  constexpr int kMaxPieces = 2;  // 16-byte pieces per thread: H <= 8192
+  const int H = p.H, G = H >> 7, n16 = H >> 4;
+  uint4 xv[kMaxPieces];
+  uint32_t cw = 0;
+  if (p.xpan) {
+    const uint4* xrow = reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H);
+#pragma unroll
+    for (int q = 0; q < kMaxPieces; ++q) {
+      const int c = tid + q * kTopkThreads;
+      xv[q] = c < n16 ? __ldcg(xrow + c) : make_uint4(0, 0, 0, 0);
+    }
+    if (tid < G)
+      cw = __ldcg(reinterpret_cast<const uint32_t*>(p.x8c + static_cast<size_t>(m) * (H >> 5)) + tid);
+  }
+
   // ---- one thread per expert: the KS partials (all loads in flight), then
   // their sum in a fixed order, the score and the choice key
 #pragma unroll
@@ -257,8 +277,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
       if (my_id < 0 || my_id >= E) my_id = 0;
       const float wgt = s_s[my_id] / ssum;
       // the token's row among the expert's rows this step (any order: an MMA
-      // output column depends on its own row only)
-      const int slot = atomicAdd(p.cnt + my_id, 1);
+      // output column depends on its own row only); a lone token's is row 0
+      const int slot = M > 1 ? atomicAdd(p.cnt + my_id, 1) : 0;
       p.route_w[m * K + lane] = wgt;
       p.ids[m * K + lane] = my_id;
       p.slots[m * K + lane] = slot;
@@ -274,10 +294,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   // (row = its slot) and of the shared expert (row = the token index): each
   // 16-byte piece is read once and stored k + 1 times
   if (p.xpan) {
-    const int H = p.H, G = H >> 7, n16 = H >> 4;
-    const uint4* xrow = reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H);
-    for (int c = tid; c < n16; c += kTopkThreads) {
-      const uint4 v = xrow[c];
+#pragma unroll
+    for (int q = 0; q < kMaxPieces; ++q) {
+      const int c = tid + q * kTopkThreads;
+      if (c >= n16) break;
+      const uint4 v = xv[q];
       for (int d = 0; d <= K; ++d) {
         const int e = d < K ? pick_s[d] : E;
         const int r = d < K ? slot_s[d] : m;
@@ -286,9 +307,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
                                   panel_byte(r, (c & 7) << 4)) = v;
       }
     }
-    const uint8_t* crow = p.x8c + static_cast<size_t>(m) * (H >> 5);
-    for (int g = tid; g < G; g += kTopkThreads) {
-      const uint32_t code = *reinterpret_cast<const uint32_t*>(crow + 4 * g);
+    if (tid < G) {
+      const int g = tid;
+      const uint32_t code = cw;
       for (int d = 0; d <= K; ++d) {
         const int e = d < K ? pick_s[d] : E;
         const int r = d < K ? slot_s[d] : m;
