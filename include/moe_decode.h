@@ -194,7 +194,8 @@ const char* moe_kernel_name(int i);
  *      byte 1024 + 128 r + 16 ((c / 16) xor (r % 8)) + c % 16. Row r of a
  *      routed expert is the token that took slot r (any order); rows of the
  *      shared expert are the tokens in order. Rows >= the expert's token
- *      count, and experts no token picked, are unspecified.
+ *      count, and experts no token picked, are unspecified; at M = 1 no
+ *      routed panel is written (every unit reads the shared expert's).
  *  MOE_REGION_H8        u8  [units][I / 128][7168] the same layout for the
  *      requantised silu(g) * u rows, by unit (MOE_REGION_ACTIVE order)
  *  MOE_REGION_PARTIAL   f32 [rows][H]  expert output rows y

@@ -372,6 +372,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   sp.dbg_normed = static_cast<__nv_bfloat16*>(d.normed);
   sp.dbg_x8 = d.x8;
   sp.dbg_x8c = d.x8_codes;
+  sp.xpan_shared = h->xpan + static_cast<size_t>(E) * (H / 128) * kPanelPitch;
   sp.H = H;
   sp.eps = h->cfg.eps;
 
@@ -425,7 +426,9 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   mark(2);
   if (err == cudaSuccess) err = launch_topk(tp, st);
   mark(3);
-  if (err == cudaSuccess) err = launch_experts(h->pe, h->num_sms, st);
+  ExpertParams pe = h->pe;
+  pe.M = M;
+  if (err == cudaSuccess) err = launch_experts(pe, h->num_sms, st);
   mark(4);
   if (err == cudaSuccess) err = launch_combine(cp, st);
   mark(5);

@@ -328,9 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         const uint32_t bytes = kABytes + pbytes;
         const bool shared_e = a.x == p.E;
         const int G = k.phase ? p.g2 : p.g13;
-        // x panels are kept per expert id, h panels per unit
+        // x panels are kept per expert id (a lone token's experts all read
+        // the shared expert's: its single row), h panels per unit
+        const int xe = p.M == 1 ? p.E : a.x;
         const uint8_t* pan = k.phase ? p.hpan + static_cast<size_t>(k.u) * G * kPanelPitch
-                                     : p.xpan + static_cast<size_t>(a.x) * G * kPanelPitch;
+                                     : p.xpan + static_cast<size_t>(xe) * G * kPanelPitch;
         auto issue_b = [&](int g, int s) {
           ptx::bulk_load(ptx::smem_u32(smem + kOffB + s * kBBytes), pan + g * kPanelPitch, pbytes,
                          ptx::smem_u32(&bars->full[s]), pol_x);

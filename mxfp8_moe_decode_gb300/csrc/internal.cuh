@@ -55,6 +55,7 @@ struct SeamParams {
   __nv_bfloat16* dbg_normed;
   uint8_t* dbg_x8;
   uint8_t* dbg_x8c;
+  uint8_t* xpan_shared;  // [H/128] x panels of the shared expert (row = token), or null
   int H;
   float eps;
 };
@@ -105,7 +106,8 @@ struct TopkParams {
   int* tok_pos;               // [M][k + 1]: partial-output row of (token, pick); pick k = shared
   const uint8_t* x8;          // [M][H] the seam's MXFP8 rows and codes [M][H/32]
   const uint8_t* x8c;
-  uint8_t* xpan;              // [E + 1][H/128] x panels by expert id (or null: no panels)
+  uint8_t* xpan;              // [E + 1][H/128] x panels by expert id (or null: no panels);
+                              // the routed ones (at M > 1; the seam writes the shared one)
   int32_t* dbg_ids;
   float* dbg_w;
   float* dbg_logits;
@@ -129,7 +131,9 @@ struct ExpertParams {
   const ActiveExpert* act;
   const uint4* sfa13;         // [E + 1][I/64][H/128] compact weight-scale entries
   const uint4* sfa2;          // [E + 1][H/128][I/128]
-  const uint8_t* xpan;        // [E + 1][H/128] x panels by expert id (written by the top-k kernel)
+  const uint8_t* xpan;        // [E + 1][H/128] x panels by expert id (the routed ones written by
+                              // the top-k kernel, the shared one -- rows = tokens -- by the seam;
+                              // at M = 1 every unit reads the shared one: its single row is token 0)
   uint8_t* hpan;              // [units][I/128] h panels by unit (written by the w13 epilogue)
   float* part;                // [rows][H]
   int* ready;                 // [E + 1]: finished w13 tiles per unit (zeroed by the top-k kernel)
@@ -141,6 +145,7 @@ struct ExpertParams {
   int t2, g2;                 // w2: tiles per unit (H/128), K stages (I/128)
   int units_max;              // capacity of the active-expert table
   int rows_max;               // capacity of the partial-output rows
+  int M;                      // this step's tokens
 };
 
 struct CombineParams {

@@ -198,7 +198,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   const int H = p.H, G = H >> 7, n16 = H >> 4;
   uint4 xv[kMaxPieces];
   uint32_t cw = 0;
-  if (p.xpan) {
+  // (a lone token's experts read the shared expert's panels, which the seam
+  // writes: nothing to store then)
+  const bool panels = p.xpan != nullptr && M > 1;
+  if (panels) {
     const uint4* xrow = reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H);
 #pragma unroll
     for (int q = 0; q < kMaxPieces; ++q) {
@@ -248,12 +251,18 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     }
   }
   __syncthreads();
+  // (four adjacent lanes per candidate, each counting over a quarter)
   const int ncand = (E >> 5) * K;
-  for (int c = tid; c < ncand; c += kTopkThreads) {
-    const unsigned long long mine = cand_s[c];
+  for (int c0 = 0; c0 < ncand; c0 += kTopkThreads / 4) {
+    const int c = c0 + (tid >> 2);
+    const bool live = c < ncand;
+    const unsigned long long mine = live ? cand_s[c] : 0ull;
     int rank = 0;
-    for (int o = 0; o < ncand; ++o) rank += cand_s[o] > mine;
-    if (rank < K) {
+    if (live)
+      for (int o = tid & 3; o < ncand; o += 4) rank += cand_s[o] > mine;
+    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+    if (live && (tid & 3) == 0 && rank < K) {
       const int ex = 0x7fffffff - static_cast<int>(static_cast<uint32_t>(mine));
       pick_s[rank] = ex;
     }
@@ -291,17 +300,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   __syncthreads();
 
   // ---- this token's MXFP8 row and codes into the x panels of its experts
-  // (row = its slot) and of the shared expert (row = the token index): each
-  // 16-byte piece is read once and stored k + 1 times
-  if (p.xpan) {
+  // (row = its slot): each 16-byte piece is read once and stored k times
+  if (panels) {
 #pragma unroll
     for (int q = 0; q < kMaxPieces; ++q) {
       const int c = tid + q * kTopkThreads;
       if (c >= n16) break;
       const uint4 v = xv[q];
-      for (int d = 0; d <= K; ++d) {
-        const int e = d < K ? pick_s[d] : E;
-        const int r = d < K ? slot_s[d] : m;
+      for (int d = 0; d < K; ++d) {
+        const int e = pick_s[d], r = slot_s[d];
         if (r < 0 || r >= kMaxTokens) continue;
         *reinterpret_cast<uint4*>(p.xpan + (static_cast<size_t>(e) * G + (c >> 3)) * kPanelPitch +
                                   panel_byte(r, (c & 7) << 4)) = v;
@@ -310,9 +317,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     if (tid < G) {
       const int g = tid;
       const uint32_t code = cw;
-      for (int d = 0; d <= K; ++d) {
-        const int e = d < K ? pick_s[d] : E;
-        const int r = d < K ? slot_s[d] : m;
+      for (int d = 0; d < K; ++d) {
+        const int e = pick_s[d], r = slot_s[d];
         if (r < 0 || r >= kMaxTokens) continue;
         *reinterpret_cast<uint32_t*>(p.xpan + (static_cast<size_t>(e) * G + g) * kPanelPitch +
                                      panel_code_byte(r)) = code;

@@ -109,6 +109,13 @@ __global__ void __launch_bounds__(kThreads) seam_kernel(const SeamParams p) {
         p.x8c[ci] = static_cast<uint8_t>(code);
         if (p.dbg_x8c) p.dbg_x8c[ci] = static_cast<uint8_t>(code);
       }
+      if (p.xpan_shared) {
+        // row t of the shared expert's x panels: the 8 code bytes at column
+        // 8 o of the panel (o >> 4), and the group's scale code in its image
+        uint8_t* pan = p.xpan_shared + static_cast<size_t>(o >> 4) * kPanelPitch;
+        *reinterpret_cast<uint2*>(pan + panel_byte(t, (o & 15) << 3)) = q;
+        if ((tid & 3) == 0) pan[panel_code_byte(t) + ((o >> 2) & 3)] = static_cast<uint8_t>(code);
+      }
     }
   }
 }
