@@ -385,6 +385,14 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   rp.E = E;
   rp.KS = h->ks;
   rp.Hs = h->hs;
+  // Small steps: the shared expert's weights go to L2 while the routing runs
+  // (at larger M the prefetch slows the top-k kernel about as much as it
+  // saves in the expert kernel).
+  const bool pf = M <= kPrefetchMaxM;
+  rp.pf_ptr[0] = pf ? static_cast<const uint8_t*>(h->w.sw13) : nullptr;  // [2 I][H] e4m3
+  rp.pf_bytes[0] = pf ? 2ull * h->cfg.inter * H : 0;
+  rp.pf_ptr[1] = pf ? static_cast<const uint8_t*>(h->w.sw2) : nullptr;  // [H][I] e4m3
+  rp.pf_bytes[1] = pf ? static_cast<uint64_t>(H) * h->cfg.inter : 0;
 
   TopkParams tp;
   tp.logit_part = h->logit_part;

@@ -297,6 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
 
   // the routing tables and the x panels come from the top-k kernel
   ptx::griddep_wait();
+  // The scheduler's first task is the CTA's index, a w13 tile whenever the
+  // step has at least as many w13 tiles as CTAs: its unit's entry is loaded
+  // together with the unit count rather than after it.
+  const int u0 = static_cast<int>(blockIdx.x) / p.t13;
+  int4 a0 = make_int4(0, 0, 0, 0);
+  if (warp == 8 && lane == 0 && u0 < p.units_max) a0 = __ldcg(reinterpret_cast<const int4*>(p.act) + u0);
   int units = __ldcg(p.counters + kCtrUnits);
   if (units < 0 || units > p.units_max) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
@@ -601,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         int4 a = make_int4(0, 0, 0, 0);
         for (; task < ntasks; task = grid + atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
           k = decode_task(task, n13, p);
-          a = __ldcg(act + k.u);
+          const bool first = j == 0 && task == static_cast<int>(blockIdx.x) && k.phase == 0;
+          a = first ? a0 : __ldcg(act + k.u);
           if (task_valid(a, p)) break;
         }
         const bool last = task >= ntasks;

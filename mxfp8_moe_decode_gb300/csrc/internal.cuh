@@ -35,6 +35,7 @@ constexpr int kCtrUnits = 2;     // active experts this step (routed + 1 shared)
 constexpr int kCtrRouted = 3;    // distinct routed experts this step
 constexpr int kCtrTasks = 4;     // expert kernel: next task to hand out (zeroed by the top-k kernel)
 constexpr int kCtrWords = 64;
+constexpr int kPrefetchMaxM = 8;  // steps of at most this many tokens prefetch the shared expert
 
 // One active expert of a step: what the expert kernels need to find its
 // weights and its token rows.
@@ -64,6 +65,12 @@ struct RouterParams {
   const __nv_bfloat16* normed;
   const __nv_bfloat16* gate_w;
   float* logit_part;  // [KS][M][E]
+  // Byte ranges (16-byte aligned, sizes multiples of 16, or null) that the
+  // CTAs prefetch into L2 (evict-last) while the routing runs: the shared
+  // expert's weights, which the expert kernel reads whatever the routing.
+  // Prefetches are issued at a limited rate per SM: each CTA takes a share.
+  const uint8_t* pf_ptr[2];
+  uint64_t pf_bytes[2];
   int M, H, E, KS, Hs;
 };
 

@@ -137,6 +137,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Bulk prefetch of global bytes into L2 (address and size multiples of 16),
+// with an L2 cache-eviction policy for the lines.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+               "r"(bytes), "l"(policy)
+               : "memory");
+}
+
 // The same with an L2 cache-eviction policy for the source lines.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar, uint64_t policy) {

@@ -111,6 +111,8 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   rp.normed = static_cast<const __nv_bfloat16*>(normed);
   rp.gate_w = static_cast<const __nv_bfloat16*>(gate_w);
   rp.logit_part = reinterpret_cast<float*>(base + o_lp);
+  rp.pf_ptr[0] = rp.pf_ptr[1] = nullptr;  // nothing to prefetch
+  rp.pf_bytes[0] = rp.pf_bytes[1] = 0;
   rp.M = M;
   rp.H = hidden;
   rp.E = experts;

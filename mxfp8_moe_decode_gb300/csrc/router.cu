@@ -119,6 +119,24 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
   }
   int never = 0;
   ptx::mbar_wait(ptx::smem_u32(&bar), 0, &never, kWaitLimitNs);
+  // ---- this CTA's share of the L2 prefetch (chunks b, b + ctas, ... of each
+  // range), issued once the CTA's own loads have landed so that it does not
+  // delay them
+  if (tid < 32) {
+    constexpr uint32_t kChunk = 32 * 1024;
+    const uint32_t ctas = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
+    const uint64_t pol = ptx::policy_evict_last();
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (!p.pf_ptr[r]) continue;
+      const uint64_t n = (p.pf_bytes[r] + kChunk - 1) / kChunk;
+      for (uint64_t c = b + ctas * static_cast<uint64_t>(tid); c < n; c += ctas * 32ull) {
+        const uint64_t off = c * kChunk;
+        const uint64_t len = p.pf_bytes[r] - off < kChunk ? p.pf_bytes[r] - off : kChunk;
+        ptx::prefetch_l2(p.pf_ptr[r] + off, static_cast<uint32_t>(len), pol);
+      }
+    }
+  }
 
   // ---- tensor-core partial products over this warp's 16-column steps
   const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group, column pair
