@@ -376,8 +376,21 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   sp.H = H;
   sp.eps = h->cfg.eps;
 
+  // Small steps run the seam inside the router kernel (each router CTA makes
+  // its K-slice of the normed rows): one kernel boundary and one pass over
+  // the normed rows less on the way to the experts.
+  const bool fuse_seam = M <= kSeamFuseMaxM && h->hs % 32 == 0;
   RouterParams rp;
   rp.normed = h->normed;
+  rp.x = fuse_seam ? sp.x : nullptr;
+  rp.norm_w = sp.norm_w;
+  rp.x8 = sp.x8;
+  rp.x8c = sp.x8c;
+  rp.xpan_shared = sp.xpan_shared;
+  rp.dbg_normed = sp.dbg_normed;
+  rp.dbg_x8 = sp.dbg_x8;
+  rp.dbg_x8c = sp.dbg_x8c;
+  rp.eps = sp.eps;
   rp.gate_w = static_cast<const __nv_bfloat16*>(h->w.gate_w);
   rp.logit_part = h->logit_part;
   rp.M = M;
@@ -428,7 +441,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   cp.K = K;
 
   mark(0);
-  if (err == cudaSuccess) err = launch_seam(sp, M, st);
+  if (err == cudaSuccess && !fuse_seam) err = launch_seam(sp, M, st);
   mark(1);
   if (err == cudaSuccess) err = launch_router(rp, st);
   mark(2);

@@ -36,6 +36,7 @@ constexpr int kCtrRouted = 3;    // distinct routed experts this step
 constexpr int kCtrTasks = 4;     // expert kernel: next task to hand out (zeroed by the top-k kernel)
 constexpr int kCtrWords = 64;
 constexpr int kPrefetchMaxM = 8;  // steps of at most this many tokens prefetch the shared expert
+constexpr int kSeamFuseMaxM = 4;  // steps of at most this many tokens run the seam in the router
 
 // One active expert of a step: what the expert kernels need to find its
 // weights and its token rows.
@@ -62,9 +63,22 @@ struct SeamParams {
 };
 
 struct RouterParams {
-  const __nv_bfloat16* normed;
+  const __nv_bfloat16* normed;  // [M][H] the seam's rows (read when x is null)
   const __nv_bfloat16* gate_w;
   float* logit_part;  // [KS][M][E]
+  // Fused seam (M <= kSeamFuseMaxM, Hs a multiple of 32): every CTA makes its
+  // K-slice of the normed rows from x itself; the CTAs of expert block 0 also
+  // write the slice's MXFP8 bytes, codes, shared-expert panel rows and the
+  // debug copies (null: not wanted).
+  const __nv_bfloat16* x;       // [M][H] hidden rows, or null: no fusion
+  const __nv_bfloat16* norm_w;  // [H]
+  uint8_t* x8;                  // [M][H]
+  uint8_t* x8c;                 // [M][H/32]
+  uint8_t* xpan_shared;         // [H/128] x panels of the shared expert
+  __nv_bfloat16* dbg_normed;
+  uint8_t* dbg_x8;
+  uint8_t* dbg_x8c;
+  float eps;
   // Byte ranges (16-byte aligned, sizes multiples of 16, or null) that the
   // CTAs prefetch into L2 (evict-last) while the routing runs: the shared
   // expert's weights, which the expert kernel reads whatever the routing.

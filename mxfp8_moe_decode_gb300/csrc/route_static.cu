@@ -111,6 +111,12 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   rp.normed = static_cast<const __nv_bfloat16*>(normed);
   rp.gate_w = static_cast<const __nv_bfloat16*>(gate_w);
   rp.logit_part = reinterpret_cast<float*>(base + o_lp);
+  rp.x = nullptr;  // the rows come normalised
+  rp.norm_w = nullptr;
+  rp.x8 = rp.x8c = rp.xpan_shared = nullptr;
+  rp.dbg_normed = nullptr;
+  rp.dbg_x8 = rp.dbg_x8c = nullptr;
+  rp.eps = 0.0f;
   rp.pf_ptr[0] = rp.pf_ptr[1] = nullptr;  // nothing to prefetch
   rp.pf_bytes[0] = rp.pf_bytes[1] = 0;
   rp.M = M;

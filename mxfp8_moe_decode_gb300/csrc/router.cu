@@ -38,6 +38,7 @@
 
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "seam.cuh"
 
 namespace moe {
 namespace {
@@ -65,6 +66,9 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a
 }
 
 constexpr int kMTiles = (kMaxTokens + 15) / 16;
+// fused seam: slice octets per thread (kSeamFuseMaxM rows of at most kMaxHs columns)
+constexpr int kFuseIters = (kSeamFuseMaxM * (kMaxHs / 8) + kThreads - 1) / kThreads;
+static_assert(kSeamFuseMaxM <= 4, "the fused seam's sums of squares take rows two at a time");
 
 __host__ __device__ constexpr int router_pitch(int Hs) { return Hs * 2 + 16; }
 
@@ -103,22 +107,110 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
     ptx::mbar_init(ptx::smem_u32(&bar), 1);
     ptx::fence_mbar_init();
   }
-  ptx::griddep_wait();  // the normed rows come from the seam kernel
+  // fused seam: the norm weight of this thread's slice octets, before waiting
+  const int nsl = Hs >> 3;  // octets of the K-slice
+  uint4 wpre[kFuseIters];
+  if (p.x) {
+#pragma unroll
+    for (int s = 0; s < kFuseIters; ++s) {
+      const int q = s * kThreads + tid;
+      wpre[s] = q < M * nsl ? __ldg(reinterpret_cast<const uint4*>(p.norm_w) + (k0 >> 3) + q % nsl)
+                            : make_uint4(0, 0, 0, 0);
+    }
+  }
+  ptx::griddep_wait();  // the normed rows (or x) come from the previous kernel
   ptx::griddep_launch_dependents();
   __syncthreads();
 
-  // ---- the K-slice of every normed row: one bulk copy per row, all in flight
-  // (rows M .. rows - 1 are left as they are: they only feed output rows that
-  // are dropped)
-  if (tid == 0) {
-    const uint32_t b = ptx::smem_u32(&bar);
-    ptx::mbar_arrive_expect_tx(b, static_cast<uint32_t>(M) * Hs * 2);
-    for (int m = 0; m < M; ++m)
-      ptx::bulk_load(ptx::smem_u32(xs + static_cast<size_t>(m) * ld),
-                     p.normed + static_cast<size_t>(m) * H + k0, Hs * 2, b);
+  if (p.x) {
+    // ---- fused seam, in the seam's arithmetic and order (seam.cuh): first
+    // every row's sum of squares -- thread t plays owner t & 127 for rows
+    // (t >> 7) and (t >> 7) + 2 -- then this CTA's K-slice of the normed rows
+    // straight into shared memory
+    __shared__ float warp_sums[kSeamFuseMaxM][4];
+    __shared__ float scale_s[kSeamFuseMaxM];
+    {
+      const int own = tid & (kSeamOwners - 1), m0 = tid >> 7, noct = H >> 3;
+      uint4 raw[2][kSeamMaxOct];
+#pragma unroll
+      for (int ps = 0; ps < 2; ++ps) {
+        const int m = m0 + 2 * ps;
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * H);
+#pragma unroll
+        for (int i = 0; i < kSeamMaxOct; ++i) {
+          const int o = own + i * kSeamOwners;
+          raw[ps][i] = m < M && o < noct ? __ldg(xr + o) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int ps = 0; ps < 2; ++ps) {
+        const int m = m0 + 2 * ps;  // the same in the whole warp
+        if (m < M) {
+          float ss = 0.0f;
+#pragma unroll
+          for (int i = 0; i < kSeamMaxOct; ++i) {
+            if (own + i * kSeamOwners < noct) {
+              float v[8];
+              unpack_bf16x8(raw[ps][i], v);
+              ss = seam_sumsq_octet(v, ss);
+            }
+          }
+          ss = seam_warp_sum(ss);
+          if (lane == 0) warp_sums[m][warp & 3] = ss;
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < M) scale_s[tid] = seam_scale(warp_sums[tid], H, p.eps);
+    __syncthreads();
+    // octet q of the slice tasks: row q / nsl, octet k0 / 8 + q % nsl; the 4
+    // octets of a 32-group are 4 adjacent lanes (nsl is a multiple of 4)
+    const bool writer = blockIdx.x == 0;
+#pragma unroll
+    for (int s = 0; s < kFuseIters; ++s) {
+      const int q0 = s * kThreads;
+      if (q0 >= M * nsl) break;  // uniform
+      const int q = q0 + tid;
+      const bool live = q < M * nsl;
+      const int m = live ? q / nsl : 0, ol = q - m * nsl, o = (k0 >> 3) + ol;
+      float v[8];
+      unpack_bf16x8(live ? __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * H) + o)
+                         : make_uint4(0, 0, 0, 0),
+                    v);
+      uint4 nv;
+      int code;
+      const uint2 q8 = seam_quant_octet(v, wpre[s], scale_s[m], &nv, &code);
+      if (live) {
+        *reinterpret_cast<uint4*>(xs + static_cast<size_t>(m) * ld + 16 * ol) = nv;
+        if (writer) {
+          const size_t row = static_cast<size_t>(m) * H;
+          reinterpret_cast<uint2*>(p.x8 + row)[o] = q8;
+          if (p.dbg_normed) reinterpret_cast<uint4*>(p.dbg_normed + row)[o] = nv;
+          if (p.dbg_x8) reinterpret_cast<uint2*>(p.dbg_x8 + row)[o] = q8;
+          if ((o & 3) == 0) {
+            const size_t ci = static_cast<size_t>(m) * (H >> 5) + (o >> 2);
+            p.x8c[ci] = static_cast<uint8_t>(code);
+            if (p.dbg_x8c) p.dbg_x8c[ci] = static_cast<uint8_t>(code);
+          }
+          seam_store_panel(p.xpan_shared, m, o, q8, code);
+        }
+      }
+    }
+    __syncthreads();
+  } else {
+    // ---- the K-slice of every normed row: one bulk copy per row, all in
+    // flight (rows M .. rows - 1 are left as they are: they only feed output
+    // rows that are dropped)
+    if (tid == 0) {
+      const uint32_t b = ptx::smem_u32(&bar);
+      ptx::mbar_arrive_expect_tx(b, static_cast<uint32_t>(M) * Hs * 2);
+      for (int m = 0; m < M; ++m)
+        ptx::bulk_load(ptx::smem_u32(xs + static_cast<size_t>(m) * ld),
+                       p.normed + static_cast<size_t>(m) * H + k0, Hs * 2, b);
+    }
+    int never = 0;
+    ptx::mbar_wait(ptx::smem_u32(&bar), 0, &never, kWaitLimitNs);
   }
-  int never = 0;
-  ptx::mbar_wait(ptx::smem_u32(&bar), 0, &never, kWaitLimitNs);
   // ---- this CTA's share of the L2 prefetch (chunks b, b + ctas, ... of each
   // range), issued once the CTA's own loads have landed so that it does not
   // delay them
