@@ -290,6 +290,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   __shared__ int pick_s[kMaxTopk];
   __shared__ int slot_s[kMaxTopk];
   __shared__ int is_last;
+  int pk_id = 0, pk_slot = 0;  // lane j < k of warp 0: pick j
+  float pk_w = 0.0f;
   static_assert(kMaxExperts <= 2 * kTopkThreads, "two experts per thread");
   // the bias does not depend on the router: fetch it before waiting
   float bias[2];
@@ -394,19 +396,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     if (lane < K) {
       int my_id = pick_s[lane];
       if (my_id < 0 || my_id >= E) my_id = 0;
-      const float wgt = s_s[my_id] / ssum;
+      pk_w = s_s[my_id] / ssum;
       // the token's row among the expert's rows this step (any order: an MMA
       // output column depends on its own row only); a lone token's is row 0
-      const int slot = M > 1 ? atomicAdd(p.cnt + my_id, 1) : 0;
-      p.route_w[m * K + lane] = wgt;
-      p.ids[m * K + lane] = my_id;
-      p.slots[m * K + lane] = slot;
+      pk_slot = M > 1 ? atomicAdd(p.cnt + my_id, 1) : 0;
+      pk_id = my_id;
       pick_s[lane] = my_id;
-      slot_s[lane] = slot;
-      if (p.dbg_w) p.dbg_w[m * K + lane] = wgt;
-      if (p.dbg_ids) p.dbg_ids[m * K + lane] = my_id;
+      slot_s[lane] = pk_slot;
     }
   }
+  // (global stores go after the barriers where they can: a block barrier
+  // waits for the stores before it)
   __syncthreads();
 
   // ---- this token's MXFP8 row and codes into the x panels of its experts
@@ -436,19 +436,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     }
   }
 
-  if (warp == 0) {
-    if (M > 1) {
-      // the last token CTA to get here builds the tables
+  if (warp == 0 && lane < K) {
+    p.route_w[m * K + lane] = pk_w;
+    p.ids[m * K + lane] = pk_id;
+    p.slots[m * K + lane] = pk_slot;
+    if (p.dbg_w) p.dbg_w[m * K + lane] = pk_w;
+    if (p.dbg_ids) p.dbg_ids[m * K + lane] = pk_id;
+  }
+  if (M > 1) {
+    // the last token CTA to get here builds the tables (this CTA's picks and
+    // slots are visible before its ticket; the panels only to the next kernel)
+    if (warp == 0) {
       __threadfence();
       __syncwarp();
       if (lane == 0) is_last = (atomicAdd(&p.counters[kCtrTicket], 1) == M - 1);
-    } else if (lane == 0) {
-      is_last = 1;
     }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
   }
-  __syncthreads();
-  if (!is_last) return;
-  if (M > 1) __threadfence();
 
   // ---- the last token CTA: every pick and slot into shared memory, the
   // per-expert row counts rebuilt there
@@ -467,10 +473,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     ids_s[tid] = pick_s[tid];
     slots_s[tid] = slot_s[tid];
   }
-  // every token CTA has taken its slots: the per-expert counters start over
-  for (int ex = tid; ex < E; ex += kTopkThreads) p.cnt[ex] = 0;
-  if (p.ready)  // the expert kernel's per-unit readiness counts start at zero
-    for (int i = tid; i < p.ready_count; i += kTopkThreads) p.ready[i] = 0;
   __syncthreads();
   for (int i = tid; i < M * K; i += kTopkThreads) {
     const int ex = ids_s[i];
@@ -501,19 +503,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     total += v;
   }
   const uint32_t excl = before + incl - mine;
-  int pos = static_cast<int>(excl >> 16), u = static_cast<int>(excl & 0xffffu);
-  if (e0 < E) {
-    base_s[e0] = pos;
-    if (n0 > 0) {
-      p.act[u] = ActiveExpert{e0, pos, n0, 0};
-      ++u;
-      pos += n0;
-    }
-  }
-  if (e1 < E) {
-    base_s[e1] = pos;
-    if (n1 > 0) p.act[u] = ActiveExpert{e1, pos, n1, 0};
-  }
+  const int pos0 = static_cast<int>(excl >> 16), u0 = static_cast<int>(excl & 0xffffu);
+  const int pos1 = pos0 + n0, u1 = u0 + (n0 > 0);
+  if (e0 < E) base_s[e0] = pos0;
+  if (e1 < E) base_s[e1] = pos1;
+  __syncthreads();
+  // ---- the tables (global writes only from here on)
+  if (e0 < E && n0 > 0) p.act[u0] = ActiveExpert{e0, pos0, n0, 0};
+  if (e1 < E && n1 > 0) p.act[u1] = ActiveExpert{e1, pos1, n1, 0};
   if (tid == 0) {
     const int routed = static_cast<int>(total & 0xffffu);
     p.act[routed] = ActiveExpert{E, static_cast<int>(total >> 16), M, 0};  // shared: rows M K..
@@ -522,7 +519,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     p.counters[kCtrTicket] = 0;  // ready for the next step
     p.counters[kCtrTasks] = 0;   // the expert kernel hands out tasks from zero
   }
-  __syncthreads();
   // partial-output row of every (token, pick): the expert's run + the slot
   for (int i = tid; i < M * K; i += kTopkThreads) {
     const int mm = i / K, j = i - mm * K;
@@ -531,6 +527,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     p.tok_pos[mm * (K + 1) + j] = base_s[ex] + sl;
   }
   for (int mm = tid; mm < M; mm += kTopkThreads) p.tok_pos[mm * (K + 1) + K] = M * K + mm;
+  // every token CTA has taken its slots: the per-expert counters start over
+  for (int ex = tid; ex < E; ex += kTopkThreads) p.cnt[ex] = 0;
+  if (p.ready)  // the expert kernel's per-unit readiness counts start at zero
+    for (int i = tid; i < p.ready_count; i += kTopkThreads) p.ready[i] = 0;
 }
 
 }  // namespace
