@@ -19,30 +19,34 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
   const int m = blockIdx.y;
   const int H = p.H, K = p.K;
   const int col = (blockIdx.x * kThreads + threadIdx.x) * 8;
-  ptx::griddep_wait();  // the routing tables and the partial rows come from earlier kernels
+  // The routing tables come from the top-k kernel, complete before this grid
+  // is launched (the expert kernel lets it launch only after waiting for
+  // top-k): they are loaded before waiting for the expert grid's partial rows.
+  int pos[kMaxTopk + 1];
+  float w[kMaxTopk + 1];
+#pragma unroll
+  for (int j = 0; j <= kMaxTopk; ++j) {
+    pos[j] = j <= K ? __ldcg(p.tok_pos + m * (K + 1) + j) : 0;
+    w[j] = j < K ? __ldcg(p.route_w + m * K + j) : 1.0f;  // the shared expert's weight is 1
+  }
+  ptx::griddep_wait();  // the partial rows come from the expert kernel
   ptx::griddep_launch_dependents();
   if (col >= H) return;
   // picks 0 .. k-1 weighted, then the shared expert (pick k), in this order;
-  // positions, weights and partial rows of up to 9 picks in flight at once
+  // the partial rows of up to 9 picks in flight at once
   constexpr int kBatch = 9;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j0 = 0; j0 <= K; j0 += kBatch) {
-    int pos[kBatch];
-    float w[kBatch];
 #pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const int j = j0 + q;
-      pos[q] = j <= K ? p.tok_pos[m * (K + 1) + j] : 0;
-      w[q] = j < K ? p.route_w[m * K + j] : 1.0f;  // the shared expert's weight is 1
-    }
+  for (int j0 = 0; j0 <= kMaxTopk; j0 += kBatch) {
+    if (j0 > K) break;
     float4 v[kBatch][2];
 #pragma unroll
     for (int q = 0; q < kBatch; ++q) {
-      if (j0 + q <= K) {
+      if (j0 + q <= K && j0 + q <= kMaxTopk) {
         const float4* src =
-            reinterpret_cast<const float4*>(p.part + static_cast<size_t>(pos[q]) * H + col);
+            reinterpret_cast<const float4*>(p.part + static_cast<size_t>(pos[j0 + q]) * H + col);
         v[q][0] = src[0];
         v[q][1] = src[1];
       }
@@ -51,14 +55,15 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     for (int q = 0; q < kBatch; ++q) {
       const int j = j0 + q;
       if (j < K) {
-        acc[0] = fmaf(w[q], v[q][0].x, acc[0]);
-        acc[1] = fmaf(w[q], v[q][0].y, acc[1]);
-        acc[2] = fmaf(w[q], v[q][0].z, acc[2]);
-        acc[3] = fmaf(w[q], v[q][0].w, acc[3]);
-        acc[4] = fmaf(w[q], v[q][1].x, acc[4]);
-        acc[5] = fmaf(w[q], v[q][1].y, acc[5]);
-        acc[6] = fmaf(w[q], v[q][1].z, acc[6]);
-        acc[7] = fmaf(w[q], v[q][1].w, acc[7]);
+        const float wj = w[j < kMaxTopk ? j : kMaxTopk];
+        acc[0] = fmaf(wj, v[q][0].x, acc[0]);
+        acc[1] = fmaf(wj, v[q][0].y, acc[1]);
+        acc[2] = fmaf(wj, v[q][0].z, acc[2]);
+        acc[3] = fmaf(wj, v[q][0].w, acc[3]);
+        acc[4] = fmaf(wj, v[q][1].x, acc[4]);
+        acc[5] = fmaf(wj, v[q][1].y, acc[5]);
+        acc[6] = fmaf(wj, v[q][1].z, acc[6]);
+        acc[7] = fmaf(wj, v[q][1].w, acc[7]);
       } else if (j == K) {
         acc[0] += v[q][0].x;
         acc[1] += v[q][0].y;

@@ -291,12 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tbase = misc->tmem_base;
-  // the next kernel may start launching: it waits for this grid before it
-  // reads anything this grid writes
-  ptx::griddep_launch_dependents();
 
   // the routing tables and the x panels come from the top-k kernel
   ptx::griddep_wait();
+  // The next kernel may start launching: it waits for this grid before it
+  // reads anything this grid writes, and may read the top-k kernel's tables
+  // at once (that grid is complete now).
+  ptx::griddep_launch_dependents();
   // The scheduler's first task is the CTA's index, a w13 tile whenever the
   // step has at least as many w13 tiles as CTAs: its unit's entry is loaded
   // together with the unit count rather than after it.
