@@ -88,7 +88,7 @@ constexpr int kTaskSlots = 8;  // task-id queue from the scheduler warp to the o
 // current task's stages are left to issue (the ring holds 8 more): late enough
 // that a w2 task is rarely claimed before its unit can be done, early enough
 // that the claim, its table read and the readiness check are over in time.
-constexpr int kClaimLead = 4;
+constexpr int kClaimLead = 10;
 
 static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "B tiles must stay 1024-aligned");
 static_assert(kBBytes >= kPanelPitch, "a panel fits its slot");
