@@ -278,6 +278,7 @@ def run_gpu(args):
         step_ms, kmean, unique, graph, out = time_layer(layer, x, dev, args.steps, args.warmup,
                                                         flush)
     clocks = clk.summary()
+    launches_per_step = layer.step_launches(wl.tokens)
     us_step = per_step_us(sum(step_ms), args.steps, world, dev)
     names = kernel_names()
     alg = W.algorithmic_bytes(d, unique)
@@ -370,7 +371,7 @@ def run_gpu(args):
         "kernel_us": {n: round(k * 1e3, 2) for n, k in zip(names, kmean)},
         "e2e": {"value": round(e2e_us, 3), "unit": "us",
                 "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2},
-        "gpu_launches": len(names) * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     if sweep:

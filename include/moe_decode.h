@@ -178,9 +178,15 @@ int moe_last_unique_experts(moe_handle* h, int* unique_routed);
  */
 int moe_set_timing_events(moe_handle* h, void* const* events, int n);
 
-/* Number of kernels one step launches, and the name of kernel i (static string). */
+/* The kernels a step can launch, in order, and the name of kernel i (static
+ * string). A step of at most 4 tokens runs the seam inside the router kernel
+ * and launches the others only (its seam events are recorded back to back). */
 int moe_kernel_count(void);
 const char* moe_kernel_name(int i);
+
+/* Number of kernels a step of M tokens launches on this handle (0 if h is
+ * null or M is out of range). */
+int moe_step_launches(const moe_handle* h, int M);
 
 /*
  * Diagnostics: device address and size of one region of the handle's scratch,

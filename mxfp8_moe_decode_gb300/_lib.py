@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
     L.moe_kernel_count.restype = ip
     L.moe_kernel_name.argtypes = [ip]
     L.moe_kernel_name.restype = ctypes.c_char_p
+    L.moe_step_launches.argtypes = [vp, ip]
+    L.moe_step_launches.restype = ip
     L.moe_scratch_region.argtypes = [vp, ip, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_size_t)]
     L.moe_scratch_region.restype = ip
     L.moe_scratch_bytes.argtypes = [vp]

@@ -148,6 +148,10 @@ class MoeDecode:
     def clear_status(self) -> int:
         return _lib.lib().moe_clear_status(self._h)
 
+    def step_launches(self, m: int) -> int:
+        """Kernels one step of m tokens launches."""
+        return _lib.lib().moe_step_launches(self._h, m)
+
     def unique_experts(self) -> int:
         v = ctypes.c_int()
         check(_lib.lib().moe_last_unique_experts(self._h, ctypes.byref(v)), "unique_experts")

@@ -134,11 +134,20 @@ int validate_weights(const moe_weights* w) {
   return MOE_OK;
 }
 
+// Small steps run the seam inside the router kernel: every router CTA makes
+// its K-slice of the normed rows (whole 32-column groups).
+bool seam_fused(const moe_handle* h, int M) { return M <= kSeamFuseMaxM && h->hs % 32 == 0; }
+
 }  // namespace
 
 extern "C" {
 
 int moe_kernel_count(void) { return kNumKernels; }
+
+int moe_step_launches(const moe_handle* h, int M) {
+  if (!h || M < 1 || M > h->cfg.max_tokens) return 0;
+  return seam_fused(h, M) ? kNumKernels - 1 : kNumKernels;
+}
 
 const char* moe_kernel_name(int i) {
   return (i >= 0 && i < kNumKernels) ? kKernelNames[i] : nullptr;
@@ -379,7 +388,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   // Small steps run the seam inside the router kernel (each router CTA makes
   // its K-slice of the normed rows): one kernel boundary and one pass over
   // the normed rows less on the way to the experts.
-  const bool fuse_seam = M <= kSeamFuseMaxM && h->hs % 32 == 0;
+  const bool fuse_seam = seam_fused(h, M);
   RouterParams rp;
   rp.normed = h->normed;
   rp.x = fuse_seam ? sp.x : nullptr;

@@ -124,6 +124,13 @@ def test_tiny_range_errors(tiny):
         assert ei.value.code == MOE_ERR_RANGE
 
 
+def test_step_launches(tiny):
+    """Steps of at most 4 tokens run the seam inside the router: one launch fewer."""
+    L = tiny.layer
+    assert [L.step_launches(m) for m in (1, 4, 5, tiny.wl.dims.max_tokens)] == [4, 4, 5, 5]
+    assert L.step_launches(0) == 0 and L.step_launches(tiny.wl.dims.max_tokens + 1) == 0
+
+
 def test_small_m4():
     L = Layer(W.WORKLOADS["small_m4"])
     try:
