@@ -410,8 +410,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   __syncthreads();
 
   // ---- this token's MXFP8 row and codes into the x panels of its experts
-  // (row = its slot): each 16-byte piece is read once and stored k times
-  if (panels) {
+  // (row = its slot): each 16-byte piece is read once and stored k times.
+  // Only the next kernel reads them, so they go out after the ticket (a fence
+  // before it would wait for them), while the last CTA builds the tables.
+  auto write_panels = [&]() {
+    if (!panels) return;
 #pragma unroll
     for (int q = 0; q < kMaxPieces; ++q) {
       const int c = tid + q * kTopkThreads;
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
                                      panel_code_byte(r)) = code;
       }
     }
-  }
+  };
 
   if (warp == 0 && lane < K) {
     p.route_w[m * K + lane] = pk_w;
@@ -445,14 +448,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   }
   if (M > 1) {
     // the last token CTA to get here builds the tables (this CTA's picks and
-    // slots are visible before its ticket; the panels only to the next kernel)
+    // slots are visible before its ticket)
     if (warp == 0) {
       __threadfence();
       __syncwarp();
       if (lane == 0) is_last = (atomicAdd(&p.counters[kCtrTicket], 1) == M - 1);
     }
     __syncthreads();
-    if (!is_last) return;
+    if (!is_last) {
+      write_panels();
+      return;
+    }
     __threadfence();
   }
 
@@ -531,6 +537,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   for (int ex = tid; ex < E; ex += kTopkThreads) p.cnt[ex] = 0;
   if (p.ready)  // the expert kernel's per-unit readiness counts start at zero
     for (int i = tid; i < p.ready_count; i += kTopkThreads) p.ready[i] = 0;
+  write_panels();  // the last token CTA's own row
 }
 
 }  // namespace
