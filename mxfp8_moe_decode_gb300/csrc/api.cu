@@ -313,6 +313,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
 
   // the expert kernel's parameter block (fixed for the handle's lifetime)
   ExpertParams& pe = h->pe;
+  pe.cnt = h->cnt;
   pe.counters = h->counters;
   pe.act = h->act;
   pe.sfa13 = h->sfa13;
@@ -410,6 +411,14 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   // Small steps: the shared expert's weights go to L2 while the routing runs
   // (at larger M the prefetch slows the top-k kernel about as much as it
   // saves in the expert kernel).
+  // the previous step's readers of the row counts, readiness counts and task
+  // counter are done once the router's grid dependency is met
+  rp.clear[0] = h->cnt;
+  rp.clear_n[0] = E;
+  rp.clear[1] = h->ready;
+  rp.clear_n[1] = h->units_max;
+  rp.clear[2] = h->counters + kCtrTasks;
+  rp.clear_n[2] = 1;
   const bool pf = M <= kPrefetchMaxM;
   rp.pf_ptr[0] = pf ? static_cast<const uint8_t*>(h->w.sw13) : nullptr;  // [2 I][H] e4m3
   rp.pf_bytes[0] = pf ? 2ull * h->cfg.inter * H : 0;
@@ -420,12 +429,8 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   tp.logit_part = h->logit_part;
   tp.bias = h->w.bias;
   tp.counters = h->counters;
-  tp.ready = h->ready;
-  tp.ready_count = E + 1;
   tp.ids = h->ids;
-  tp.act = h->act;
   tp.route_w = h->route_w;
-  tp.tok_pos = h->tok_pos;
   tp.slots = h->slots;
   tp.cnt = h->cnt;
   tp.x8 = h->x8;
@@ -443,11 +448,15 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   CombineParams cp;
   cp.part = h->part;
   cp.route_w = h->route_w;
+  cp.ids = h->ids;
+  cp.slots = h->slots;
+  cp.cnt = h->cnt;
   cp.tok_pos = h->tok_pos;
   cp.out = static_cast<__nv_bfloat16*>(out);
   cp.M = M;
   cp.H = H;
   cp.K = K;
+  cp.E = E;
 
   mark(0);
   if (err == cudaSuccess && !fuse_seam) err = launch_seam(sp, M, st);
@@ -458,6 +467,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   mark(3);
   ExpertParams pe = h->pe;
   pe.M = M;
+  pe.K = K;
   if (err == cudaSuccess) err = launch_experts(pe, h->num_sms, st);
   mark(4);
   if (err == cudaSuccess) err = launch_combine(cp, st);

@@ -19,16 +19,63 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
   const int m = blockIdx.y;
   const int H = p.H, K = p.K;
   const int col = (blockIdx.x * kThreads + threadIdx.x) * 8;
-  // The routing tables come from the top-k kernel, complete before this grid
-  // is launched (the expert kernel lets it launch only after waiting for
-  // top-k): they are loaded before waiting for the expert grid's partial rows.
-  int pos[kMaxTopk + 1];
-  float w[kMaxTopk + 1];
+  // The picks, slots and per-expert row counts come from the top-k kernel,
+  // complete before this grid is launched (the expert kernel lets it launch
+  // only after waiting for top-k). Before waiting for the expert grid's
+  // partial rows, every CTA lays out the step's units from the counts as the
+  // expert kernel does (pack_unit: one block-wide exclusive scan of the rows
+  // in expert order) and finds its token's partial-output rows.
+  __shared__ uint16_t first_s[kMaxExperts];  // (small: this CTA shares an SM with an expert CTA)
+  __shared__ uint8_t rows_s[kMaxExperts];
+  __shared__ int warp_s[kThreads / 32];
+  __shared__ int pos_s[kMaxTopk + 1];
+  static_assert(kMaxExperts <= 4 * kThreads, "four experts per thread");
+  {
+    int n[4], sum = 0;
 #pragma unroll
-  for (int j = 0; j <= kMaxTopk; ++j) {
-    pos[j] = j <= K ? __ldcg(p.tok_pos + m * (K + 1) + j) : 0;
-    w[j] = j < K ? __ldcg(p.route_w + m * K + j) : 1.0f;  // the shared expert's weight is 1
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * static_cast<int>(threadIdx.x) + i;
+      n[i] = e < p.E ? __ldcg(p.cnt + e) : 0;
+      sum += n[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if ((threadIdx.x & 31) >= off) incl += o;
+    }
+    if ((threadIdx.x & 31) == 31) warp_s[threadIdx.x >> 5] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w = 0; w < static_cast<int>(threadIdx.x >> 5); ++w) run += warp_s[w];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * static_cast<int>(threadIdx.x) + i;
+      if (e < p.E) {
+        first_s[e] = static_cast<uint16_t>(run);
+        rows_s[e] = static_cast<uint8_t>(n[i] < 255 ? n[i] : 255);
+      }
+      run += n[i];
+    }
   }
+  __syncthreads();
+  if (static_cast<int>(threadIdx.x) <= K) {
+    const int j = threadIdx.x;
+    int pos = p.M * K + m;  // pick k: the shared expert's row of this token
+    if (j < K) {
+      const int e = __ldcg(p.ids + m * K + j), sl = __ldcg(p.slots + m * K + j);
+      pos = e >= 0 && e < p.E && sl >= 0 && sl < rows_s[e] ? first_s[e] + sl : 0;
+    }
+    pos_s[j] = pos;
+    if (blockIdx.x == 0) p.tok_pos[m * (K + 1) + j] = pos;  // diagnostics
+  }
+  float w[kMaxTopk];
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) w[j] = j < K ? __ldcg(p.route_w + m * K + j) : 0.0f;
+  __syncthreads();
+  int pos[kMaxTopk + 1];
+#pragma unroll
+  for (int j = 0; j <= kMaxTopk; ++j) pos[j] = j <= K ? pos_s[j] : 0;
   ptx::griddep_wait();  // the partial rows come from the expert kernel
   ptx::griddep_launch_dependents();
   if (col >= H) return;
@@ -55,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     for (int q = 0; q < kBatch; ++q) {
       const int j = j0 + q;
       if (j < K) {
-        const float wj = w[j < kMaxTopk ? j : kMaxTopk];
+        const float wj = w[j < kMaxTopk ? j : kMaxTopk - 1];
         acc[0] = fmaf(wj, v[q][0].x, acc[0]);
         acc[1] = fmaf(wj, v[q][0].y, acc[1]);
         acc[2] = fmaf(wj, v[q][0].z, acc[2]);

@@ -77,7 +77,9 @@ constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffXchg = kOffSfa + kStages * kImgBytes;
 constexpr uint32_t kOffBar = kOffXchg + 2 * kMaxTokens * 64 * 4;  // gate and up values
 constexpr uint32_t kOffMisc = kOffBar + 512;
-constexpr uint32_t kSmemUsed = kOffMisc + 256;
+constexpr uint32_t kOffUnits = kOffMisc + 256;                     // packed unit entries
+constexpr uint32_t kOffScan = kOffUnits + ((kMaxExperts + 1) * 4 + 15) / 16 * 16;  // warp sums
+constexpr uint32_t kSmemUsed = kOffScan + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 // TMEM: 2 task buffers x 2 issuers x 64 accumulator columns, then 8 scale columns per stage
 constexpr uint32_t kTmemCols = 512;
@@ -292,26 +294,71 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
   ptx::tc_fence_after();
   const uint32_t tbase = misc->tmem_base;
 
-  // the routing tables and the x panels come from the top-k kernel
+  // the routing (row counts) and the x panels come from the top-k kernel
   ptx::griddep_wait();
   // The next kernel may start launching: it waits for this grid before it
   // reads anything this grid writes, and may read the top-k kernel's tables
   // at once (that grid is complete now).
   ptx::griddep_launch_dependents();
-  // The scheduler's first task is the CTA's index, a w13 tile whenever the
-  // step has at least as many w13 tiles as CTAs: its unit's entry is loaded
-  // together with the unit count rather than after it.
-  const int u0 = static_cast<int>(blockIdx.x) / p.t13;
-  int4 a0 = make_int4(0, 0, 0, 0);
-  if (warp == 8 && lane == 0 && u0 < p.units_max) a0 = __ldcg(reinterpret_cast<const int4*>(p.act) + u0);
-  int units = __ldcg(p.counters + kCtrUnits);
-  if (units < 0 || units > p.units_max) {
-    if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
-    units = 0;
+
+  // ---- the step's units (pack_unit) from the per-expert row counts: thread t
+  // (< 256) owns experts 2t and 2t + 1; one block-wide exclusive scan of
+  // (rows << 16 | active experts) gives each active expert its unit index and
+  // first row; the shared expert is the last unit
+  uint32_t* unit_s = reinterpret_cast<uint32_t*>(smem + kOffUnits);
+  int units;
+  {
+    uint32_t* scan_s = reinterpret_cast<uint32_t*>(smem + kOffScan);
+    const int e0 = 2 * static_cast<int>(threadIdx.x), e1 = e0 + 1;
+    int n0 = e0 < p.E ? __ldcg(p.cnt + e0) : 0;
+    int n1 = e1 < p.E ? __ldcg(p.cnt + e1) : 0;
+    if (n0 < 0 || n0 > kMaxTokens || n1 < 0 || n1 > kMaxTokens) {
+      atomicOr(p.err, kErrBounds);
+      n0 = n1 = 0;
+    }
+    const uint32_t mine = (static_cast<uint32_t>(n0 + n1) << 16) | ((n0 > 0) + (n1 > 0));
+    uint32_t incl = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) scan_s[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const uint32_t v = scan_s[w];
+      before += w < warp ? v : 0u;
+      total += v;
+    }
+    const uint32_t excl = before + incl - mine;
+    const int first = static_cast<int>(excl >> 16), u = static_cast<int>(excl & 0xffffu);
+    const int routed = static_cast<int>(total & 0xffffu);
+    units = routed + 1;
+    if (units > p.units_max || static_cast<int>(total >> 16) > p.M * p.K) {
+      if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
+      units = 0;
+    } else {
+      if (n0 > 0) unit_s[u] = pack_unit(e0, n0, first);
+      if (n1 > 0) unit_s[u + (n0 > 0)] = pack_unit(e1, n1, first + n0);
+      if (threadIdx.x == 0) unit_s[routed] = pack_unit(p.E, p.M, p.M * p.K);
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {  // the table for diagnostics
+      for (int i = threadIdx.x; i < units; i += kThreads) {
+        const uint32_t v = unit_s[i];
+        p.act[i] = ActiveExpert{static_cast<int>(v & 1023u), static_cast<int>(v >> 16),
+                                static_cast<int>((v >> 10) & 63u), 0};
+      }
+      if (threadIdx.x == 0) {
+        p.counters[kCtrUnits] = units;
+        p.counters[kCtrRouted] = units > 0 ? units - 1 : 0;
+      }
+    }
   }
   const int n13 = units * p.t13;
   const int ntasks = units * (p.t13 + p.t2);
-  const int4* act = reinterpret_cast<const int4*>(p.act);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -608,8 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         int4 a = make_int4(0, 0, 0, 0);
         for (; task < ntasks; task = grid + atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
           k = decode_task(task, n13, p);
-          const bool first = j == 0 && task == static_cast<int>(blockIdx.x) && k.phase == 0;
-          a = first ? a0 : __ldcg(act + k.u);
+          const uint32_t v = unit_s[k.u];  // (expert id, first row, rows)
+          a = make_int4(static_cast<int>(v & 1023u), static_cast<int>(v >> 16),
+                        static_cast<int>((v >> 10) & 63u), 0);
           if (task_valid(a, p)) break;
         }
         const bool last = task >= ntasks;

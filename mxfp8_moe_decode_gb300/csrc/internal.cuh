@@ -30,7 +30,6 @@ constexpr int kErrBounds = 2;
 
 // counters region (int32 words at the start of the scratch)
 constexpr int kCtrErr = 0;       // device error word (bit set)
-constexpr int kCtrTicket = 1;    // top-k: token CTAs done
 constexpr int kCtrUnits = 2;     // active experts this step (routed + 1 shared)
 constexpr int kCtrRouted = 3;    // distinct routed experts this step
 constexpr int kCtrTasks = 4;     // expert kernel: next task to hand out (zeroed by the top-k kernel)
@@ -85,6 +84,12 @@ struct RouterParams {
   // Prefetches are issued at a limited rate per SM: each CTA takes a share.
   const uint8_t* pf_ptr[2];
   uint64_t pf_bytes[2];
+  // int arrays (or null) that CTA (0, 0) sets to zero once the previous
+  // kernel is complete -- the previous step's readers of the per-expert row
+  // counts, the readiness counts and the task counter are done by then, and
+  // this step's top-k kernel runs after this grid
+  int* clear[3];
+  int clear_n[3];
   int M, H, E, KS, Hs;
 };
 
@@ -117,14 +122,10 @@ struct TopkParams {
   const float* logit_part;    // [KS][M][E]
   const float* bias;
   int* counters;
-  int* ready;                 // the expert kernel's per-unit readiness counts to clear (or null)
-  int ready_count;            // entries in ready
-  int* cnt;                   // [E + 1]: rows taken per expert this step (zero between steps)
+  int* cnt;                   // [E]: rows taken per expert this step (zero before the step)
   int* ids;                   // [M][k]
   int* slots;                 // [M][k]: the token's row among the expert's rows
-  ActiveExpert* act;          // [E + 1]
   float* route_w;             // [M][k]
-  int* tok_pos;               // [M][k + 1]: partial-output row of (token, pick); pick k = shared
   const uint8_t* x8;          // [M][H] the seam's MXFP8 rows and codes [M][H/32]
   const uint8_t* x8c;
   uint8_t* xpan;              // [E + 1][H/128] x panels by expert id (or null: no panels);
@@ -148,8 +149,9 @@ struct ExpertParams {
   CUtensorMap tm_w13_shared;  // shared w13 as [2 halves][I][H]
   CUtensorMap tm_w2;          // routed w2 as [E H rows][I]
   CUtensorMap tm_w2_shared;   // shared w2 [H][I]
-  const int* counters;
-  const ActiveExpert* act;
+  const int* cnt;             // [E]: each routed expert's rows this step (top-k's counts)
+  int* counters;              // the step's unit counts go to kCtrUnits / kCtrRouted (diagnostics)
+  ActiveExpert* act;          // [units] the unit table, written by CTA 0 (diagnostics)
   const uint4* sfa13;         // [E + 1][I/64][H/128] compact weight-scale entries
   const uint4* sfa2;          // [E + 1][H/128][I/128]
   const uint8_t* xpan;        // [E + 1][H/128] x panels by expert id (the routed ones written by
@@ -157,8 +159,8 @@ struct ExpertParams {
                               // at M = 1 every unit reads the shared one: its single row is token 0)
   uint8_t* hpan;              // [units][I/128] h panels by unit (written by the w13 epilogue)
   float* part;                // [rows][H]
-  int* ready;                 // [E + 1]: finished w13 tiles per unit (zeroed by the top-k kernel)
-  int* task_ctr;              // next task id to hand out (zeroed by the top-k kernel)
+  int* ready;                 // [units_max]: finished w13 tiles per unit (zeroed by the router)
+  int* task_ctr;              // next task id to hand out (zeroed by the router)
   int* err;
   int E;                      // routed experts (index E = shared)
   int inter, hidden;
@@ -166,15 +168,32 @@ struct ExpertParams {
   int t2, g2;                 // w2: tiles per unit (H/128), K stages (I/128)
   int units_max;              // capacity of the active-expert table
   int rows_max;               // capacity of the partial-output rows
-  int M;                      // this step's tokens
+  int M, K;                   // this step's tokens, picks per token
 };
+
+// The step's units, as every expert CTA and every combine CTA derives them
+// from the per-expert row counts: the routed experts with rows in increasing
+// id, each owning a run of partial-output rows that starts at the sum of the
+// rows of the experts before it, then the shared expert with the M tokens at
+// rows M k .. M k + M - 1. Packed unit entry: expert id (bits 0-9), rows
+// (10-15), first row (16-31).
+__host__ __device__ __forceinline__ uint32_t pack_unit(int e, int rows, int first) {
+  return static_cast<uint32_t>(e) | (static_cast<uint32_t>(rows) << 10) |
+         (static_cast<uint32_t>(first) << 16);
+}
+static_assert(kMaxExperts < 1024 && kMaxTokens < 64 && kMaxTokens * (kMaxTopk + 1) < 65536,
+              "unit entries fit 32 bits");
 
 struct CombineParams {
   const float* part;
-  const float* route_w;
-  const int* tok_pos;
+  const float* route_w;       // [M][k]
+  const int* ids;             // [M][k] picked experts
+  const int* slots;           // [M][k] the token's row among the expert's rows
+  const int* cnt;             // [E] each routed expert's rows this step
+  int* tok_pos;               // [M][k + 1] partial-output row of (token, pick), written for
+                              // diagnostics (pick k = the shared expert)
   __nv_bfloat16* out;
-  int M, H, K;
+  int M, H, K, E;
 };
 
 struct SfaPackParams {

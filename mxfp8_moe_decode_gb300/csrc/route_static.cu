@@ -79,10 +79,8 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
 
   // layout inside the static array; refuse problems that do not fit
   const size_t o_ctr = 0;
-  const size_t o_act = o_ctr + align256(kCtrWords * 4);
-  const size_t o_rw = o_act + align256(static_cast<size_t>(experts + 1) * sizeof(ActiveExpert));
-  const size_t o_tp = o_rw + align256(static_cast<size_t>(M) * topk * 4);
-  const size_t o_sl = o_tp + align256(static_cast<size_t>(M) * (topk + 1) * 4);
+  const size_t o_rw = o_ctr + align256(kCtrWords * 4);
+  const size_t o_sl = o_rw + align256(static_cast<size_t>(M) * topk * 4);
   const size_t o_cn = o_sl + align256(static_cast<size_t>(M) * topk * 4);
   const size_t o_id = o_cn + align256(static_cast<size_t>(experts + 1) * 4);
   const size_t o_lp = o_id + align256(static_cast<size_t>(M) * topk * 4);
@@ -100,8 +98,8 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   uint8_t* base = static_cast<uint8_t*>(base_v);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // the top-k ticket, the error word and the per-expert row counters must
-  // start at zero; the array keeps whatever the previous call left
+  // the error word and the per-expert row counters must start at zero; the
+  // array keeps whatever the previous call left
   if (cudaMemsetAsync(base + o_ctr, 0, kCtrWords * 4, st) != cudaSuccess ||
       cudaMemsetAsync(base + o_cn, 0, static_cast<size_t>(experts + 1) * 4, st) != cudaSuccess) {
     cudaGetLastError();
@@ -118,6 +116,10 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   rp.dbg_x8 = rp.dbg_x8c = nullptr;
   rp.eps = 0.0f;
   rp.pf_ptr[0] = rp.pf_ptr[1] = nullptr;  // nothing to prefetch
+  for (int r = 0; r < 3; ++r) {  // the memsets above clear the counters
+    rp.clear[r] = nullptr;
+    rp.clear_n[r] = 0;
+  }
   rp.pf_bytes[0] = rp.pf_bytes[1] = 0;
   rp.M = M;
   rp.H = hidden;
@@ -128,12 +130,8 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   tp.logit_part = rp.logit_part;
   tp.bias = bias;
   tp.counters = reinterpret_cast<int*>(base + o_ctr);
-  tp.ready = nullptr;
-  tp.ready_count = 0;
   tp.ids = reinterpret_cast<int*>(base + o_id);
-  tp.act = reinterpret_cast<ActiveExpert*>(base + o_act);
   tp.route_w = reinterpret_cast<float*>(base + o_rw);
-  tp.tok_pos = reinterpret_cast<int*>(base + o_tp);
   tp.slots = reinterpret_cast<int*>(base + o_sl);
   tp.cnt = reinterpret_cast<int*>(base + o_cn);
   tp.x8 = nullptr;

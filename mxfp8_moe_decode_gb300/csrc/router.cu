@@ -21,18 +21,17 @@
 //
 // topk_kernel: one CTA per token. A thread per expert sums the KS partial
 // logits in a fixed order (all partial loads issued before the sum), takes
-// sigmoid and score + bias; warp 0 picks the k largest choices with 64-bit
-// keys (order-preserving bits of the choice, then the inverted expert index,
-// so equal choices go to the lower index), one warp-wide max per pick; lane j
-// keeps pick j and takes the token's row (slot) among the expert's rows with an
-// atomic on a per-expert counter; then the CTA writes the token's MXFP8 row and
-// codes into the x panels of its k experts and of the shared expert (row =
-// token index) -- the panels are the expert kernel's B operand. The last token
-// CTA (a device-scope ticket; a single token CTA needs none) compacts: it
-// counts each expert's rows from all picks in shared memory, then one
-// block-wide scan gives the active experts in increasing id each a contiguous
-// run of partial-output rows, the shared expert last with all M tokens; it
-// clears the counters and the ticket.
+// sigmoid and score + bias and forms a 64-bit key (order-preserving bits of
+// the choice, then the inverted expert index, so equal choices go to the
+// lower index); the k largest keys are found by rank (rank within each group
+// of 32 experts, then among the groups' candidates). Lane j of warp 0 keeps
+// pick j and takes the token's row (slot) among the expert's rows with an
+// atomic on the expert's row counter (a lone token's slots are 0 and it sets
+// the counts); then the CTA writes the token's MXFP8 row and codes into the x
+// panels of its k experts (the expert kernel's B operand; the seam writes the
+// shared expert's, and a lone token's experts read that one). The per-expert
+// row counts are all the expert and combine kernels need to lay out the
+// step's units (see pack_unit); the router clears them before the next step.
 #include <cfloat>
 #include <cmath>
 
@@ -120,6 +119,12 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
   }
   ptx::griddep_wait();  // the normed rows (or x) come from the previous kernel
   ptx::griddep_launch_dependents();
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+#pragma unroll
+    for (int r = 0; r < 3; ++r)
+      if (p.clear[r])
+        for (int i = tid; i < p.clear_n[r]; i += kThreads) p.clear[r][i] = 0;
+  }
   __syncthreads();
 
   if (p.x) {
@@ -289,7 +294,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   __shared__ float s_s[kMaxExperts];
   __shared__ int pick_s[kMaxTopk];
   __shared__ int slot_s[kMaxTopk];
-  __shared__ int is_last;
   int pk_id = 0, pk_slot = 0;  // lane j < k of warp 0: pick j
   float pk_w = 0.0f;
   static_assert(kMaxExperts <= 2 * kTopkThreads, "two experts per thread");
@@ -443,101 +447,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     p.route_w[m * K + lane] = pk_w;
     p.ids[m * K + lane] = pk_id;
     p.slots[m * K + lane] = pk_slot;
+    if (M == 1) p.cnt[pk_id] = 1;  // (a lone token takes no slot atomics)
     if (p.dbg_w) p.dbg_w[m * K + lane] = pk_w;
     if (p.dbg_ids) p.dbg_ids[m * K + lane] = pk_id;
   }
-  if (M > 1) {
-    // the last token CTA to get here builds the tables (this CTA's picks and
-    // slots are visible before its ticket)
-    if (warp == 0) {
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) is_last = (atomicAdd(&p.counters[kCtrTicket], 1) == M - 1);
-    }
-    __syncthreads();
-    if (!is_last) {
-      write_panels();
-      return;
-    }
-    __threadfence();
-  }
-
-  // ---- the last token CTA: every pick and slot into shared memory, the
-  // per-expert row counts rebuilt there
-  __shared__ int base_s[kMaxExperts];
-  __shared__ int cnt_s[kMaxExperts];
-  __shared__ int ids_s[kMaxTokens * kMaxTopk];
-  __shared__ int slots_s[kMaxTokens * kMaxTopk];
-  __shared__ uint32_t wsum_s[kTopkThreads / 32];
-  for (int ex = tid; ex < E; ex += kTopkThreads) cnt_s[ex] = 0;
-  if (M > 1) {
-    for (int i = tid; i < M * K; i += kTopkThreads) {
-      ids_s[i] = __ldcg(p.ids + i);
-      slots_s[i] = __ldcg(p.slots + i);
-    }
-  } else if (tid < K) {
-    ids_s[tid] = pick_s[tid];
-    slots_s[tid] = slot_s[tid];
-  }
-  __syncthreads();
-  for (int i = tid; i < M * K; i += kTopkThreads) {
-    const int ex = ids_s[i];
-    if (ex >= 0 && ex < E) atomicAdd(&cnt_s[ex], 1);
-  }
-  __syncthreads();
-
-  // ---- active experts in increasing id and their row runs: thread t owns
-  // experts 2t and 2t + 1; one block-wide exclusive scan of (rows << 16 | active)
-  static_assert(kMaxTokens * kMaxTopk < (1 << 16), "row count fits 16 bits");
-  const int e0 = 2 * tid, e1 = 2 * tid + 1;
-  const int n0 = e0 < E ? cnt_s[e0] : 0;
-  const int n1 = e1 < E ? cnt_s[e1] : 0;
-  const uint32_t mine = (static_cast<uint32_t>(n0 + n1) << 16) | ((n0 > 0) + (n1 > 0));
-  uint32_t incl = mine;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  if (lane == 31) wsum_s[warp] = incl;
-  __syncthreads();
-  uint32_t before = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < kTopkThreads / 32; ++w) {
-    const uint32_t v = wsum_s[w];
-    before += w < warp ? v : 0u;
-    total += v;
-  }
-  const uint32_t excl = before + incl - mine;
-  const int pos0 = static_cast<int>(excl >> 16), u0 = static_cast<int>(excl & 0xffffu);
-  const int pos1 = pos0 + n0, u1 = u0 + (n0 > 0);
-  if (e0 < E) base_s[e0] = pos0;
-  if (e1 < E) base_s[e1] = pos1;
-  __syncthreads();
-  // ---- the tables (global writes only from here on)
-  if (e0 < E && n0 > 0) p.act[u0] = ActiveExpert{e0, pos0, n0, 0};
-  if (e1 < E && n1 > 0) p.act[u1] = ActiveExpert{e1, pos1, n1, 0};
-  if (tid == 0) {
-    const int routed = static_cast<int>(total & 0xffffu);
-    p.act[routed] = ActiveExpert{E, static_cast<int>(total >> 16), M, 0};  // shared: rows M K..
-    p.counters[kCtrUnits] = routed + 1;
-    p.counters[kCtrRouted] = routed;
-    p.counters[kCtrTicket] = 0;  // ready for the next step
-    p.counters[kCtrTasks] = 0;   // the expert kernel hands out tasks from zero
-  }
-  // partial-output row of every (token, pick): the expert's run + the slot
-  for (int i = tid; i < M * K; i += kTopkThreads) {
-    const int mm = i / K, j = i - mm * K;
-    const int ex = ids_s[i], sl = slots_s[i];
-    if (ex < 0 || ex >= E || sl < 0 || sl >= cnt_s[ex]) continue;
-    p.tok_pos[mm * (K + 1) + j] = base_s[ex] + sl;
-  }
-  for (int mm = tid; mm < M; mm += kTopkThreads) p.tok_pos[mm * (K + 1) + K] = M * K + mm;
-  // every token CTA has taken its slots: the per-expert counters start over
-  for (int ex = tid; ex < E; ex += kTopkThreads) p.cnt[ex] = 0;
-  if (p.ready)  // the expert kernel's per-unit readiness counts start at zero
-    for (int i = tid; i < p.ready_count; i += kTopkThreads) p.ready[i] = 0;
-  write_panels();  // the last token CTA's own row
+  write_panels();
 }
 
 }  // namespace
