@@ -419,6 +419,12 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   rp.clear_n[1] = h->units_max;
   rp.clear[2] = h->counters + kCtrTasks;
   rp.clear_n[2] = 1;
+  // small steps: the last round of w2 tiles runs as K-halves added into the
+  // step's partial rows, which start at zero
+  const int g2 = h->cfg.inter / 128;
+  const bool split = M <= kW2SplitMaxM && g2 >= 4 && g2 % 2 == 0;
+  rp.zero_rows = split ? h->part : nullptr;
+  rp.zero_n = split ? static_cast<size_t>(M) * (K + 1) * H : 0;
   const bool pf = M <= kPrefetchMaxM;
   rp.pf_ptr[0] = pf ? static_cast<const uint8_t*>(h->w.sw13) : nullptr;  // [2 I][H] e4m3
   rp.pf_bytes[0] = pf ? 2ull * h->cfg.inter * H : 0;
@@ -468,6 +474,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   ExpertParams pe = h->pe;
   pe.M = M;
   pe.K = K;
+  pe.split_tiles = split ? h->num_sms : 0;
   if (err == cudaSuccess) err = launch_experts(pe, h->num_sms, st);
   mark(4);
   if (err == cudaSuccess) err = launch_combine(cp, st);

@@ -147,20 +147,37 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 struct Task {
-  int phase;  // 0: w13, 1: w2
-  int u;      // unit (active expert)
-  int t;      // tile within the unit
+  int phase;   // 0: w13, 1: w2
+  int u;       // unit (active expert)
+  int t;       // tile within the unit
+  int g0, gn;  // the task's K stages: g0 .. g0 + gn - 1
+  int half;    // 1: a K-half of a w2 tile, added into rows that start at zero
 };
 
-__device__ __forceinline__ Task decode_task(int task, int n13, const ExpertParams& p) {
+// Task ids: every unit's w13 tiles (n13), the first w2full w2 tiles whole,
+// then the remaining w2 tiles (at most one per CTA: the launch's last round)
+// each as two K-halves. The halves even out the end of the launch: a CTA
+// that would otherwise take one more whole tile takes half of one.
+__device__ __forceinline__ Task decode_task(int task, int n13, int w2full, const ExpertParams& p) {
   Task k;
+  k.g0 = 0;
+  k.half = 0;
   if (task < n13) {
     k.phase = 0;
     k.u = task / p.t13;
     k.t = task - k.u * p.t13;
+    k.gn = p.g13;
   } else {
-    const int j = task - n13;
+    int j = task - n13;
     k.phase = 1;
+    k.gn = p.g2;
+    if (j >= w2full) {
+      const int h = j - w2full;
+      j = w2full + (h >> 1);
+      k.half = 1;
+      k.gn = p.g2 >> 1;
+      k.g0 = (h & 1) * k.gn;
+    }
     k.u = j / p.t2;
     k.t = j - k.u * p.t2;
   }
@@ -358,7 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     }
   }
   const int n13 = units * p.t13;
-  const int ntasks = units * (p.t13 + p.t2);
+  const int n2 = units * p.t2;
+  const int w2full = n2 > p.split_tiles ? n2 - p.split_tiles : 0;  // the rest go in halves
+  const int ntasks = n13 + w2full + 2 * (n2 - w2full);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -376,17 +395,20 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         int4 a;
         const int task = take_task(bars, misc, j, abort, &a);
         if (task < 0) break;  // -1: no more tasks; -2: a wait gave up
-        const Task k = decode_task(task, n13, p);
+        const Task k = decode_task(task, n13, w2full, p);
         const int nt = (a.z + 15) & ~15;
         const uint32_t pbytes = kPanelRows + nt * 128;  // the panel's used part
         const uint32_t bytes = kABytes + pbytes;
         const bool shared_e = a.x == p.E;
-        const int G = k.phase ? p.g2 : p.g13;
+        const int G = k.gn;
+        const int panels = k.phase ? p.g2 : p.g13;  // per unit (h) or expert (x)
         // x panels are kept per expert id (a lone token's experts all read
         // the shared expert's: its single row), h panels per unit
         const int xe = p.M == 1 ? p.E : a.x;
-        const uint8_t* pan = k.phase ? p.hpan + static_cast<size_t>(k.u) * G * kPanelPitch
-                                     : p.xpan + static_cast<size_t>(xe) * G * kPanelPitch;
+        const uint8_t* pan =
+            (k.phase ? p.hpan + static_cast<size_t>(k.u) * panels * kPanelPitch
+                     : p.xpan + static_cast<size_t>(xe) * panels * kPanelPitch) +
+            static_cast<size_t>(k.g0) * kPanelPitch;
         auto issue_b = [&](int g, int s) {
           ptx::bulk_load(ptx::smem_u32(smem + kOffB + s * kBBytes), pan + g * kPanelPitch, pbytes,
                          ptx::smem_u32(&bars->full[s]), pol_x);
@@ -406,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           const uint32_t full = ptx::smem_u32(&bars->full[s]);
           ptx::mbar_arrive_expect_tx(full, bytes);
           const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
-          const int x = g * kStageK;
+          const int x = (k.g0 + g) * kStageK;
           if (k.phase == 0) {
             // one box: the 64 gate rows (half 2e) over the matching 64 up rows (half 2e + 1)
             ptx::tma_load_3d(sa, shared_e ? &p.tm_w13_shared : &p.tm_w13, x, 64 * k.t,
@@ -464,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         int4 a;
         const int task = take_task(bars, misc, j, abort, &a);
         if (task < 0) break;
-        const Task k = decode_task(task, n13, p);
+        const Task k = decode_task(task, n13, w2full, p);
         const int nt = (a.z + 15) & ~15;
-        const int G = k.phase ? p.g2 : p.g13;
+        const int G = k.gn;  // at least 2: both issuers write their accumulator
         const int acc = lt & 1;
         const uint32_t use = static_cast<uint32_t>(lt) >> 1;
         ++lt;
@@ -521,10 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       task = __shfl_sync(0xffffffffu, task, 0);
       if (task < 0) break;
       const int ex = __shfl_sync(0xffffffffu, a.x, 0);  // the unit's expert id
-      const Task k = decode_task(task, n13, p);
-      const int G = k.phase ? p.g2 : p.g13;
-      const uint4* sfa = k.phase ? p.sfa2 + (static_cast<size_t>(ex) * p.t2 + k.t) * G
-                                 : p.sfa13 + (static_cast<size_t>(ex) * p.t13 + k.t) * G;
+      const Task k = decode_task(task, n13, w2full, p);
+      const int G = k.gn;
+      const uint4* sfa = (k.phase ? p.sfa2 + (static_cast<size_t>(ex) * p.t2 + k.t) * p.g2
+                                  : p.sfa13 + (static_cast<size_t>(ex) * p.t13 + k.t) * p.g13) +
+                         k.g0;
       const uint4 zero = make_uint4(0, 0, 0, 0);
       const uint4 e0 = lane < G ? __ldg(sfa + lane) : zero;  // stages lane and lane + 32
       const uint4 e1 = lane + 32 < G ? __ldg(sfa + lane + 32) : zero;
@@ -561,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       epi_bar();
       const int task = *reinterpret_cast<volatile int*>(&misc->epi_task);
       if (task < 0) break;
-      const Task k = decode_task(task, n13, p);
+      const Task k = decode_task(task, n13, w2full, p);
       const int4 a = misc->epi_act;
       const int rows = a.z;
       const int nt = (rows + 15) & ~15;
@@ -597,9 +620,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
 
       if (k.phase == 1) {
         float* dst = p.part + static_cast<size_t>(a.y) * p.hidden + kTileM * k.t + 32 * q + lane;
+        if (k.half) {
+          // the two halves' reductions onto zero give the same sum in either
+          // order (halves only in steps of at most kW2SplitMaxM tokens)
 #pragma unroll
-        for (int n = 0; n < kMaxTokens; ++n)
-          if (n < rows) dst[static_cast<size_t>(n) * p.hidden] = v[n];
+          for (int n = 0; n < kW2SplitMaxM; ++n)
+            if (n < rows) atomicAdd(dst + static_cast<size_t>(n) * p.hidden, v[n]);
+        } else {
+#pragma unroll
+          for (int n = 0; n < kMaxTokens; ++n)
+            if (n < rows) dst[static_cast<size_t>(n) * p.hidden] = v[n];
+        }
         epi_bar();
       } else {
         // gate (warps 4-5) and up (warps 6-7) values to shared memory, then
@@ -651,10 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       const int grid = static_cast<int>(gridDim.x);
       int task = static_cast<int>(blockIdx.x);
       for (uint32_t j = 0;; ++j) {
-        Task k = {0, 0, 0};
+        Task k = {0, 0, 0, 0, 0, 0};
         int4 a = make_int4(0, 0, 0, 0);
         for (; task < ntasks; task = grid + atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
-          k = decode_task(task, n13, p);
+          k = decode_task(task, n13, w2full, p);
           const uint32_t v = unit_s[k.u];  // (expert id, first row, rows)
           a = make_int4(static_cast<int>(v & 1023u), static_cast<int>(v >> 16),
                         static_cast<int>((v >> 10) & 63u), 0);

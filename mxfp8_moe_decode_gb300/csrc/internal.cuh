@@ -34,6 +34,7 @@ constexpr int kCtrUnits = 2;     // active experts this step (routed + 1 shared)
 constexpr int kCtrRouted = 3;    // distinct routed experts this step
 constexpr int kCtrTasks = 4;     // expert kernel: next task to hand out (zeroed by the top-k kernel)
 constexpr int kCtrWords = 64;
+constexpr int kW2SplitMaxM = 4;  // steps of at most this many tokens split their last w2 tiles
 constexpr int kPrefetchMaxM = 8;  // steps of at most this many tokens prefetch the shared expert
 constexpr int kSeamFuseMaxM = 4;  // steps of at most this many tokens run the seam in the router
 
@@ -90,6 +91,8 @@ struct RouterParams {
   // this step's top-k kernel runs after this grid
   int* clear[3];
   int clear_n[3];
+  float* zero_rows;  // floats all CTAs set to zero (the partial rows that w2 halves add into), or null
+  size_t zero_n;
   int M, H, E, KS, Hs;
 };
 
@@ -166,6 +169,9 @@ struct ExpertParams {
   int inter, hidden;
   int t13, g13;               // w13: tiles per unit (I/64), K stages (H/128)
   int t2, g2;                 // w2: tiles per unit (H/128), K stages (I/128)
+  int split_tiles;            // the step's last w2 tiles (at most this many) run as two K-halves
+                              // added into zeroed rows (0: none; only steps of <= kW2SplitMaxM
+                              // tokens, g2 >= 4)
   int units_max;              // capacity of the active-expert table
   int rows_max;               // capacity of the partial-output rows
   int M, K;                   // this step's tokens, picks per token

@@ -120,6 +120,8 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
     rp.clear[r] = nullptr;
     rp.clear_n[r] = 0;
   }
+  rp.zero_rows = nullptr;
+  rp.zero_n = 0;
   rp.pf_bytes[0] = rp.pf_bytes[1] = 0;
   rp.M = M;
   rp.H = hidden;

@@ -125,6 +125,12 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
       if (p.clear[r])
         for (int i = tid; i < p.clear_n[r]; i += kThreads) p.clear[r][i] = 0;
   }
+  if (p.zero_rows) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * gridDim.y * kThreads;
+    for (size_t i = (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * kThreads + tid;
+         i < p.zero_n; i += stride)
+      p.zero_rows[i] = 0.0f;
+  }
   __syncthreads();
 
   if (p.x) {
