@@ -182,11 +182,15 @@ def capture(layer, x, dev, events=None):
 
 
 def time_layer(layer, x, dev, steps: int, warmup: int, flush):
-    """Graph-replay timing. The step time comes from a graph without timing
-    events (kernels overlap through programmatic dependent launch); the
-    per-kernel breakdown from a second graph with an event node between
-    kernels. L2 is flushed (untimed) before every replay.
-    Returns (per-step ms, per-kernel mean ms, unique routed, graph, out)."""
+    """Graph-replay timing, L2 flushed (untimed) before every replay. The step
+    time is taken by two event nodes inside the step's graph, just before its
+    first kernel and after its last (the kernels still overlap through
+    programmatic dependent launch; the graph's own launch latency is outside);
+    the same graph replayed between stream events gives the replay time,
+    launch latency included. The per-kernel breakdown comes from a third
+    graph with an event node between kernels.
+    Returns (per-step ms, per-kernel mean ms, unique routed, graph, out,
+    per-replay ms)."""
     import torch
 
     from mxfp8_moe_decode_gb300 import kernel_names
@@ -204,14 +208,26 @@ def time_layer(layer, x, dev, steps: int, warmup: int, flush):
         g.replay()
     torch.cuda.synchronize(dev)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms = []
+    replay_ms = []
     for _ in range(steps):
         flush()
         t0.record(cur)
         g.replay()
         t1.record(cur)
         t1.synchronize()
-        step_ms.append(t0.elapsed_time(t1))
+        replay_ms.append(t0.elapsed_time(t1))
+
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    gb, _ = capture(layer, x, dev, events=eb)
+    step_ms = []
+    for i in range(warmup + steps):
+        flush()
+        gb.replay()
+        eb[1].synchronize()
+        if i >= warmup:
+            step_ms.append(eb[0].elapsed_time(eb[1]))
+    torch.cuda.synchronize(dev)
+    del gb  # the graph holds record nodes of `eb`: drop it before the events
 
     nk = len(kernel_names())
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
@@ -230,7 +246,7 @@ def time_layer(layer, x, dev, steps: int, warmup: int, flush):
     if layer.status() != 0:
         raise RuntimeError(f"device status {layer.status()}")
     kmean = [statistics.mean(k) for k in kern]
-    return step_ms, kmean, unique, g, out
+    return step_ms, kmean, unique, g, out, replay_ms
 
 
 def per_step_us(total_ms: float, steps: int, world: int, device=None) -> float:
@@ -275,8 +291,8 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     with Clocks(local) as clk:
-        step_ms, kmean, unique, graph, out = time_layer(layer, x, dev, args.steps, args.warmup,
-                                                        flush)
+        step_ms, kmean, unique, graph, out, replay_ms = time_layer(layer, x, dev, args.steps,
+                                                                   args.warmup, flush)
     clocks = clk.summary()
     launches_per_step = layer.step_launches(wl.tokens)
     us_step = per_step_us(sum(step_ms), args.steps, world, dev)
@@ -330,12 +346,13 @@ def run_gpu(args):
                 prev_ew = None
                 torch.cuda.empty_cache()
             L2, x2, ew2 = make_layer(swl, dev, ew=reuse)
-            ms, km, u2, g2, _ = time_layer(L2, x2, dev, max(5, args.steps // 2), 3, flush)
+            ms, km, u2, g2, _, rms = time_layer(L2, x2, dev, max(5, args.steps // 2), 3, flush)
             del g2
             us2 = statistics.mean(ms) * 1e3
             a2 = W.algorithmic_bytes(swl.dims, u2)
             e2 = (u2 + 1) * swl.dims.expert_bytes()
             sweep[name] = {"M": swl.tokens, "us_per_step": round(us2, 2),
+                           "replay_us_per_step": round(statistics.mean(rms) * 1e3, 2),
                            "unique_routed": u2, "alg_bytes": a2,
                            "step_gbs": round(a2 / (us2 * 1e-6) / 1e9, 1),
                            "step_frac": round(a2 / (us2 * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
@@ -364,8 +381,11 @@ def run_gpu(args):
                    "alg_bytes_per_step": alg, "step_gbs": round(step_gbs, 1) if step_gbs else None,
                    "step_frac_of_peak": round(step_gbs / peaks["hbm_gbs"], 4) if step_gbs else None,
                    "l2": "flushed (512 MB write) before every timed step; weights > L2",
-                   "timing": "CUDA-graph replay, CUDA events per step; kernel_us from a second graph "
-                  "with event nodes between kernels",
+                   "timing": "CUDA-graph replay; the step is timed by event nodes inside its graph "
+                             "just before its first kernel and after its last (replay_us_per_step: the "
+                             "same graph between stream events, graph launch latency included); "
+                             "kernel_us from a graph with event nodes between kernels",
+                   "replay_us_per_step": round(statistics.mean(replay_ms) * 1e3, 3),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline,
         "kernel_us": {n: round(k * 1e3, 2) for n, k in zip(names, kmean)},

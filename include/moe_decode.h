@@ -172,6 +172,9 @@ int moe_last_unique_experts(moe_handle* h, int* unique_routed);
  * Timing hooks for profiling: while set, every step records events[i]
  * (cudaEvent_t values, caller-owned) on its stream just before kernel i and
  * events[n_kernels] after the last kernel; n must equal moe_kernel_count()+1.
+ * With n = 2, events[0] is recorded just before the step's first kernel and
+ * events[1] after its last, and nothing in between (the kernels keep
+ * overlapping through programmatic dependent launch).
  * Pass events = NULL, n = 0 to turn it off. Inside a stream capture the
  * records become event-record nodes of the graph: the events must then outlive
  * every graph (and graph exec) captured with them.

@@ -172,7 +172,8 @@ class MoeDecode:
         return _lib.lib().moe_scratch_bytes(self._h)
 
     def set_timing_events(self, events) -> None:
-        """events: list of moe_kernel_count()+1 torch.cuda.Event (or None to stop)."""
+        """events: moe_kernel_count()+1 torch.cuda.Event (one before each kernel and
+        one after the last), or 2 (the step's start and end), or None to stop."""
         L = _lib.lib()
         if events is None:
             check(L.moe_set_timing_events(self._h, None, 0), "set_timing_events")

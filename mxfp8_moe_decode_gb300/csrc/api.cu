@@ -359,7 +359,8 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
   const int H = h->cfg.hidden, E = h->cfg.experts, K = h->cfg.topk;
-  const bool timed = h->n_events == kNumKernels + 1;
+  // per-kernel events (kNumKernels + 1), or two that bracket the step
+  const bool timed = h->n_events == kNumKernels + 1 || h->n_events == 2;
   cudaError_t err = cudaSuccess;
   // under stream capture a plain record only adds a dependency; an external
   // record becomes an event-record node that fires at every graph replay
@@ -370,7 +371,12 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
     if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
   }
   auto mark = [&](int i) {
-    if (timed && err == cudaSuccess) err = cudaEventRecordWithFlags(h->events[i], st, rec_flags);
+    if (!timed || err != cudaSuccess) return;
+    if (h->n_events == 2) {  // the step's start and end only
+      if (i == 0 || i == kNumKernels) err = cudaEventRecordWithFlags(h->events[i ? 1 : 0], st, rec_flags);
+      return;
+    }
+    err = cudaEventRecordWithFlags(h->events[i], st, rec_flags);
   };
 
   SeamParams sp;
@@ -531,7 +537,7 @@ int moe_set_timing_events(moe_handle* h, void* const* events, int n) {
     h->n_events = 0;
     return MOE_OK;
   }
-  if (n != kNumKernels + 1) return MOE_ERR_ARG;
+  if (n != kNumKernels + 1 && n != 2) return MOE_ERR_ARG;
   for (int i = 0; i < n; ++i) {
     if (!events[i]) return MOE_ERR_ARG;
     h->events[i] = static_cast<cudaEvent_t>(events[i]);
