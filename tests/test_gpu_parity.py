@@ -124,6 +124,43 @@ def test_tiny_range_errors(tiny):
         assert ei.value.code == MOE_ERR_RANGE
 
 
+@pytest.mark.parametrize("name,m", [("tiny_m1", 1), ("small_m4", 4), ("tiny_m1", 7)])
+def test_unit_table(name, m):
+    """The unit table the expert kernel derives from the per-expert row counts
+    (written by its CTA 0) and the partial-output row of every pick the
+    combine derives from the same counts (MOE_REGION_TOKPOS): routed experts
+    with rows in increasing id, contiguous row runs from 0 in that order, the
+    shared expert last with rows M k .. M k + M - 1; a pick's row lies in its
+    expert's run and the picks of one expert fill the run exactly."""
+    from mxfp8_moe_decode_gb300._lib import REGION_ACTIVE, REGION_TOKPOS
+    L = Layer(W.WORKLOADS[name])
+    try:
+        d = L.wl.dims
+        x, _ = gapped_tokens(L.wl, L.ri, m=m)
+        _, dbg = L.run(x)
+        ids = dbg["topk_ids"].numpy()
+        K, E = d.topk, d.experts
+        counts = np.bincount(ids.reshape(-1), minlength=E)
+        active = np.nonzero(counts)[0]
+        units = len(active) + 1
+        assert L.layer.unique_experts() == len(active)
+        act = L.layer.scratch_region(REGION_ACTIVE, torch.int32).numpy().reshape(-1, 4)[:units]
+        first = np.concatenate([[0], np.cumsum(counts[active])])
+        np.testing.assert_array_equal(act[:-1, 0], active)
+        np.testing.assert_array_equal(act[:-1, 1], first[:-1])
+        np.testing.assert_array_equal(act[:-1, 2], counts[active])
+        assert tuple(act[-1, :3]) == (E, m * K, m)
+        pos = L.layer.scratch_region(REGION_TOKPOS, torch.int32).numpy()[: m * (K + 1)]
+        pos = pos.reshape(m, K + 1)
+        np.testing.assert_array_equal(pos[:, K], m * K + np.arange(m))
+        start = dict(zip(active.tolist(), first[:-1].tolist()))
+        for e in active.tolist():
+            rows = np.sort(pos[:, :K][ids == e])
+            np.testing.assert_array_equal(rows, start[e] + np.arange(counts[e]))
+    finally:
+        L.close()
+
+
 def test_step_launches(tiny):
     """Steps of at most 4 tokens run the seam inside the router: one launch fewer."""
     L = tiny.layer
