@@ -106,7 +106,7 @@ struct Bars {
   uint64_t tempty[2];
   uint64_t drain;
   uint64_t task_full[kTaskSlots];   // the producer posted a task id
-  uint64_t task_empty[kTaskSlots];  // both MMA issuers, the helper warp and the epilogue read it
+  uint64_t task_empty[kTaskSlots];  // its five readers (kTaskReaders) have taken it
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
 
@@ -250,7 +250,8 @@ __device__ __forceinline__ int ld_acquire_cta(const int* p) {
   return v;
 }
 
-// Bounded wait until the helper warp has published task j as ready.
+// Bounded wait until a shared-memory sequence number reaches j (the
+// scheduler's readiness news, the producer's progress).
 __device__ __forceinline__ bool wait_seq(const int* seq, int j, volatile int* abort) {
   if (ld_acquire_cta(seq) >= j) return true;
   const uint64_t t0 = ptx::globaltimer_ns();

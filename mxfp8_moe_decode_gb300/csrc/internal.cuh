@@ -32,7 +32,7 @@ constexpr int kErrBounds = 2;
 constexpr int kCtrErr = 0;       // device error word (bit set)
 constexpr int kCtrUnits = 2;     // active experts this step (routed + 1 shared)
 constexpr int kCtrRouted = 3;    // distinct routed experts this step
-constexpr int kCtrTasks = 4;     // expert kernel: next task to hand out (zeroed by the top-k kernel)
+constexpr int kCtrTasks = 4;     // expert kernel: next task to hand out (zeroed by the router)
 constexpr int kCtrWords = 64;
 constexpr int kW2SplitMaxM = 4;  // steps of at most this many tokens split their last w2 tiles
 constexpr int kPrefetchMaxM = 8;  // steps of at most this many tokens prefetch the shared expert

@@ -421,8 +421,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
 
   // ---- this token's MXFP8 row and codes into the x panels of its experts
   // (row = its slot): each 16-byte piece is read once and stored k times.
-  // Only the next kernel reads them, so they go out after the ticket (a fence
-  // before it would wait for them), while the last CTA builds the tables.
+  // Only the next kernel reads them: they go out last, after the picks.
   auto write_panels = [&]() {
     if (!panels) return;
 #pragma unroll
