@@ -249,6 +249,15 @@ def time_layer(layer, x, dev, steps: int, warmup: int, flush):
     return step_ms, kmean, unique, g, out, replay_ms
 
 
+def kernel_table(names, ms, launches: int) -> dict:
+    """Per-kernel µs; a step that launches one kernel fewer runs the seam in
+    the router (its seam events bracket nothing: reported as null)."""
+    out = {n: round(k * 1e3, 2) for n, k in zip(names, ms)}
+    if launches == len(names) - 1 and "seam" in out:
+        out["seam"] = None
+    return out
+
+
 def per_step_us(total_ms: float, steps: int, world: int, device=None) -> float:
     """Whole-job microseconds per step: the slowest rank's timed total (a MAX
     all-reduce over the process group when world > 1) over the steps all
@@ -357,7 +366,7 @@ def run_gpu(args):
                            "step_gbs": round(a2 / (us2 * 1e-6) / 1e9, 1),
                            "step_frac": round(a2 / (us2 * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                            "experts_gbs": round(e2 / (km[ix] * 1e-3) / 1e9, 1),
-                           "kernel_us": {n: round(k * 1e3, 2) for n, k in zip(names, km)}}
+                           "kernel_us": kernel_table(names, km, L2.step_launches(swl.tokens))}
             L2.close()
             del L2
             prev_seed, prev_ew = swl.seed, ew2
@@ -388,7 +397,7 @@ def run_gpu(args):
                    "replay_us_per_step": round(statistics.mean(replay_ms) * 1e3, 3),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline,
-        "kernel_us": {n: round(k * 1e3, 2) for n, k in zip(names, kmean)},
+        "kernel_us": kernel_table(names, kmean, launches_per_step),
         "e2e": {"value": round(e2e_us, 3), "unit": "us",
                 "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2},
         "gpu_launches": launches_per_step * args.steps,
