@@ -60,6 +60,9 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+NOMINAL_GBS = 8000.0  # GB300 HBM3e nominal bandwidth: the metric's "% of 8 TB/s"
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in ("expert.cu", "ptx.cuh", "mx.cuh", "internal.cuh"):
@@ -365,6 +368,7 @@ def run_gpu(args):
                            "unique_routed": u2, "alg_bytes": a2,
                            "step_gbs": round(a2 / (us2 * 1e-6) / 1e9, 1),
                            "step_frac": round(a2 / (us2 * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                           "step_frac_of_8tbs": round(a2 / (us2 * 1e-6) / 1e9 / NOMINAL_GBS, 4),
                            "experts_gbs": round(e2 / (km[ix] * 1e-3) / 1e9, 1),
                            "kernel_us": kernel_table(names, km, L2.step_launches(swl.tokens))}
             L2.close()
@@ -389,6 +393,8 @@ def run_gpu(args):
                    "shared_experts": 1, "unique_routed_experts": unique,
                    "alg_bytes_per_step": alg, "step_gbs": round(step_gbs, 1) if step_gbs else None,
                    "step_frac_of_peak": round(step_gbs / peaks["hbm_gbs"], 4) if step_gbs else None,
+                   "step_frac_of_8tbs": round(step_gbs / NOMINAL_GBS, 4) if step_gbs else None,
+                   "median_us_per_step": round(statistics.median(step_ms) * 1e3, 3),
                    "l2": "flushed (512 MB write) before every timed step; weights > L2",
                    "timing": "CUDA-graph replay; the step is timed by event nodes inside its graph "
                              "just before its first kernel and after its last (replay_us_per_step: the "
