@@ -424,6 +424,23 @@ def run_gpu(args):
 _CPU_WEIGHTS: dict = {}
 
 
+def blas_threads() -> str:
+    """The numpy BLAS thread count the oracle runs with (threadpoolctl where
+    installed, else the usual environment variables, else the library default)."""
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return str(n[0])
+    except Exception:  # noqa: BLE001 - optional package
+        pass
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v):
+            return os.environ[v]
+    return "library default"
+
+
 def cpu_baseline(wl, n_experts: int, unique: int | None = None, repeats: int = 1) -> dict:
     """The oracle, as it stands, on the host cores: the seam and router on all M
     rows plus the expert path of a sample of the touched experts (dequantise +
@@ -464,7 +481,7 @@ def cpu_baseline(wl, n_experts: int, unique: int | None = None, repeats: int = 1
     per_expert = t_exp / max(1, len(sample))
     est_s = t_front + per_expert * (u + 1)
     return {"value": round(est_s * 1e6, 1), "unit": "us", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
+            "blas_threads": blas_threads(), "kind": "oracle",
             "sample": f"{wl.name}: seam + router on all {x.shape[0]} rows, then the fp64 expert "
                       f"path of {len(sample)} of the {u} touched routed experts "
                       f"({per_expert:.2f} s each), scaled to {u} + 1 shared experts"}
