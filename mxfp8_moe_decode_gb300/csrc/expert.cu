@@ -57,9 +57,9 @@
 // kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
 //
 // Launched with programmatic dependent launch: the prologue (barriers, TMEM,
-// tensor-map prefetch) runs while the top-k kernel finishes; everything else
-// waits for it (griddepcontrol.wait) -- the weights to stream depend on the
-// routing it writes.
+// tensor-map prefetch) runs while the top-k kernel finishes; the scheduler
+// warp then waits for it (griddepcontrol.wait) -- the weights to stream depend
+// on the routing it writes -- and every other role waits on the task queue.
 #include "internal.cuh"
 #include "mx.cuh"
 #include "ptx.cuh"
@@ -77,9 +77,8 @@ constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffXchg = kOffSfa + kStages * kImgBytes;
 constexpr uint32_t kOffBar = kOffXchg + 2 * kMaxTokens * 64 * 4;  // gate and up values
 constexpr uint32_t kOffMisc = kOffBar + 512;
-constexpr uint32_t kOffUnits = kOffMisc + 256;                     // packed unit entries
-constexpr uint32_t kOffScan = kOffUnits + ((kMaxExperts + 1) * 4 + 15) / 16 * 16;  // warp sums
-constexpr uint32_t kSmemUsed = kOffScan + 64;
+constexpr uint32_t kOffUnits = kOffMisc + 512;                     // packed unit entries
+constexpr uint32_t kSmemUsed = kOffUnits + ((kMaxExperts + 1) * 4 + 15) / 16 * 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
 // TMEM: 2 task buffers x 2 issuers x 64 accumulator columns, then 8 scale columns per stage
 constexpr uint32_t kTmemCols = 512;
@@ -112,7 +111,9 @@ static_assert(sizeof(Bars) <= 512, "barrier area");
 
 struct Misc {
   int4 slot_act[kTaskSlots];  // the posted task's unit entry (expert id, first row, rows)
+  int4 slot_task[kTaskSlots]; // the posted task, decoded (pack_task)
   int4 epi_act;
+  int4 epi_k;
   uint32_t tmem_base;
   int abort;
   int epi_ok;
@@ -121,7 +122,7 @@ struct Misc {
   int prod_seq;   // the last task (sequence number) the producer has taken
   int task_slot[kTaskSlots];
 };
-static_assert(sizeof(Misc) <= 256, "misc area");
+static_assert(sizeof(Misc) <= 512, "misc area");
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -212,30 +213,57 @@ __device__ __forceinline__ bool wait_ready(const int* ctr, int target, volatile 
 // with its unit's table entry; each of the five readers takes both and frees
 // the slot at once. A reader gets -2 when a wait gave up (the abort flag is set).
 constexpr int kTaskReaders = 5;  // producer, two MMA issuers, scale-image warp, epilogue
+// A decoded task in 16 bytes: phase, half and tile; unit; first stage and
+// stage count.
+__device__ __forceinline__ int4 pack_task(const Task& k) {
+  return make_int4(k.phase | (k.half << 1) | (k.t << 2), k.u, k.g0 | (k.gn << 16), 0);
+}
+__device__ __forceinline__ Task unpack_task(int4 v) {
+  Task k;
+  k.phase = v.x & 1;
+  k.half = (v.x >> 1) & 1;
+  k.t = v.x >> 2;
+  k.u = v.y;
+  k.g0 = v.z & 0xffff;
+  k.gn = v.z >> 16;
+  return k;
+}
+
+__device__ __forceinline__ void st_v4(volatile int4* dst, int4 v) {
+  dst->x = v.x;
+  dst->y = v.y;
+  dst->z = v.z;
+  dst->w = v.w;
+}
+__device__ __forceinline__ int4 ld_v4(const volatile int4* src) {
+  return make_int4(src->x, src->y, src->z, src->w);
+}
+
+// The j-th task of this CTA: the scheduler posts its id (-1: no more tasks)
+// with the task decoded and its unit's table entry; each of the five readers
+// takes them and frees the slot at once. A reader gets -2 when a wait gave up
+// (the abort flag is set).
 __device__ __forceinline__ bool post_task(Bars* bars, Misc* misc, uint32_t j, int task, int4 a,
-                                          volatile int* abort) {
+                                          int4 kt, volatile int* abort) {
   const int q = static_cast<int>(j % kTaskSlots);
   const uint32_t round = j / kTaskSlots;
   if (!ptx::mbar_wait(ptx::smem_u32(&bars->task_empty[q]), (round & 1) ^ 1, abort, kWaitLimitNs))
     return false;
   *reinterpret_cast<volatile int*>(&misc->task_slot[q]) = task;
-  volatile int4* dst = &misc->slot_act[q];
-  dst->x = a.x;
-  dst->y = a.y;
-  dst->z = a.z;
-  dst->w = a.w;
+  st_v4(&misc->slot_act[q], a);
+  st_v4(&misc->slot_task[q], kt);
   ptx::mbar_arrive(ptx::smem_u32(&bars->task_full[q]));
   return true;
 }
 
 __device__ __forceinline__ int take_task(Bars* bars, Misc* misc, uint32_t j, volatile int* abort,
-                                         int4* a) {
+                                         int4* a, Task* k) {
   const int q = static_cast<int>(j % kTaskSlots);
   const uint32_t round = j / kTaskSlots;
   if (!ptx::mbar_wait(ptx::smem_u32(&bars->task_full[q]), round & 1, abort, kWaitLimitNs)) return -2;
   const int task = *reinterpret_cast<volatile int*>(&misc->task_slot[q]);
-  const volatile int4* src = &misc->slot_act[q];
-  *a = make_int4(src->x, src->y, src->z, src->w);
+  *a = ld_v4(&misc->slot_act[q]);
+  *k = unpack_task(ld_v4(&misc->slot_task[q]));
   ptx::mbar_arrive(ptx::smem_u32(&bars->task_empty[q]));
   return task;
 }
@@ -312,74 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
   ptx::tc_fence_after();
   const uint32_t tbase = misc->tmem_base;
 
-  // the routing (row counts) and the x panels come from the top-k kernel
-  ptx::griddep_wait();
-  // The next kernel may start launching: it waits for this grid before it
-  // reads anything this grid writes, and may read the top-k kernel's tables
-  // at once (that grid is complete now).
-  ptx::griddep_launch_dependents();
-
-  // ---- the step's units (pack_unit) from the per-expert row counts: thread t
-  // (< 256) owns experts 2t and 2t + 1; one block-wide exclusive scan of
-  // (rows << 16 | active experts) gives each active expert its unit index and
-  // first row; the shared expert is the last unit
   uint32_t* unit_s = reinterpret_cast<uint32_t*>(smem + kOffUnits);
-  int units;
-  {
-    uint32_t* scan_s = reinterpret_cast<uint32_t*>(smem + kOffScan);
-    const int e0 = 2 * static_cast<int>(threadIdx.x), e1 = e0 + 1;
-    int n0 = e0 < p.E ? __ldcg(p.cnt + e0) : 0;
-    int n1 = e1 < p.E ? __ldcg(p.cnt + e1) : 0;
-    if (n0 < 0 || n0 > kMaxTokens || n1 < 0 || n1 > kMaxTokens) {
-      atomicOr(p.err, kErrBounds);
-      n0 = n1 = 0;
-    }
-    const uint32_t mine = (static_cast<uint32_t>(n0 + n1) << 16) | ((n0 > 0) + (n1 > 0));
-    uint32_t incl = mine;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    if (lane == 31) scan_s[warp] = incl;
-    __syncthreads();
-    uint32_t before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
-      const uint32_t v = scan_s[w];
-      before += w < warp ? v : 0u;
-      total += v;
-    }
-    const uint32_t excl = before + incl - mine;
-    const int first = static_cast<int>(excl >> 16), u = static_cast<int>(excl & 0xffffu);
-    const int routed = static_cast<int>(total & 0xffffu);
-    units = routed + 1;
-    if (units > p.units_max || static_cast<int>(total >> 16) > p.M * p.K) {
-      if (threadIdx.x == 0) atomicOr(p.err, kErrBounds);
-      units = 0;
-    } else {
-      if (n0 > 0) unit_s[u] = pack_unit(e0, n0, first);
-      if (n1 > 0) unit_s[u + (n0 > 0)] = pack_unit(e1, n1, first + n0);
-      if (threadIdx.x == 0) unit_s[routed] = pack_unit(p.E, p.M, p.M * p.K);
-    }
-    __syncthreads();
-    if (blockIdx.x == 0) {  // the table for diagnostics
-      for (int i = threadIdx.x; i < units; i += kThreads) {
-        const uint32_t v = unit_s[i];
-        p.act[i] = ActiveExpert{static_cast<int>(v & 1023u), static_cast<int>(v >> 16),
-                                static_cast<int>((v >> 10) & 63u), 0};
-      }
-      if (threadIdx.x == 0) {
-        p.counters[kCtrUnits] = units;
-        p.counters[kCtrRouted] = units > 0 ? units - 1 : 0;
-      }
-    }
-  }
-  const int n13 = units * p.t13;
-  const int n2 = units * p.t2;
-  const int w2full = n2 > p.split_tiles ? n2 - p.split_tiles : 0;  // the rest go in halves
-  const int ntasks = n13 + w2full + 2 * (n2 - w2full);
-
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -394,9 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       // shared memory; they go out as soon as it has.
       for (uint32_t j = 0; ok; ++j) {
         int4 a;
-        const int task = take_task(bars, misc, j, abort, &a);
+        Task k;
+        const int task = take_task(bars, misc, j, abort, &a, &k);
         if (task < 0) break;  // -1: no more tasks; -2: a wait gave up
-        const Task k = decode_task(task, n13, w2full, p);
         const int nt = (a.z + 15) & ~15;
         const uint32_t pbytes = kPanelRows + nt * 128;  // the panel's used part
         const uint32_t bytes = kABytes + pbytes;
@@ -485,9 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       bool ok = true;
       for (uint32_t j = 0; ok; ++j) {
         int4 a;
-        const int task = take_task(bars, misc, j, abort, &a);
+        Task k;
+        const int task = take_task(bars, misc, j, abort, &a, &k);
         if (task < 0) break;
-        const Task k = decode_task(task, n13, w2full, p);
         const int nt = (a.z + 15) & ~15;
         const int G = k.gn;  // at least 2: both issuers write their accumulator
         const int acc = lt & 1;
@@ -540,11 +501,18 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     bool ok = true;
     for (uint32_t j = 0; ok; ++j) {
       int4 a = make_int4(0, 0, 0, 0);
-      int task = lane == 0 ? take_task(bars, misc, j, abort, &a) : 0;
+      Task k0 = {0, 0, 0, 0, 0, 0};
+      int task = lane == 0 ? take_task(bars, misc, j, abort, &a, &k0) : 0;
       task = __shfl_sync(0xffffffffu, task, 0);
       if (task < 0) break;
       const int ex = __shfl_sync(0xffffffffu, a.x, 0);  // the unit's expert id
-      const Task k = decode_task(task, n13, w2full, p);
+      Task k;
+      k.phase = __shfl_sync(0xffffffffu, k0.phase, 0);
+      k.u = __shfl_sync(0xffffffffu, k0.u, 0);
+      k.t = __shfl_sync(0xffffffffu, k0.t, 0);
+      k.g0 = __shfl_sync(0xffffffffu, k0.g0, 0);
+      k.gn = __shfl_sync(0xffffffffu, k0.gn, 0);
+      k.half = __shfl_sync(0xffffffffu, k0.half, 0);
       const int G = k.gn;
       const uint4* sfa = (k.phase ? p.sfa2 + (static_cast<size_t>(ex) * p.t2 + k.t) * p.g2
                                   : p.sfa13 + (static_cast<size_t>(ex) * p.t13 + k.t) * p.g13) +
@@ -579,13 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     for (uint32_t j = 0;; ++j) {
       if (threadIdx.x == 128) {
         int4 ta;
-        misc->epi_task = take_task(bars, misc, j, abort, &ta);
+        Task tk;
+        misc->epi_task = take_task(bars, misc, j, abort, &ta, &tk);
         misc->epi_act = ta;
+        misc->epi_k = pack_task(tk);
       }
       epi_bar();
       const int task = *reinterpret_cast<volatile int*>(&misc->epi_task);
       if (task < 0) break;
-      const Task k = decode_task(task, n13, w2full, p);
+      const Task k = unpack_task(misc->epi_k);
       const int4 a = misc->epi_act;
       const int rows = a.z;
       const int nt = (rows + 15) & ~15;
@@ -673,16 +643,109 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ scheduler
+    // The shared expert is unit 0 in every step, with the fixed entry (E,
+    // first row M K, M rows), and its x panels come from the seam, two kernels
+    // back (complete once this grid runs: the top-k kernel lets it launch only
+    // after its own wait). So its w13 tiles need no routing: CTA b < t13 posts
+    // tile b at once, and it streams while the top-k kernel finishes.
+    const int grid = static_cast<int>(gridDim.x);
+    const bool pre = static_cast<int>(blockIdx.x) < p.t13;
+    bool pre_ok = true;
+    if (pre && lane == 0) {
+      const Task k0 = {0, 0, static_cast<int>(blockIdx.x), 0, p.g13, 0};
+      pre_ok = post_task(bars, misc, 0, static_cast<int>(blockIdx.x),
+                         make_int4(p.E, p.M * p.K, p.M, 0), pack_task(k0), abort);
+      if (pre_ok) st_release_cta(&misc->ready_seq, 0);
+    }
+    // The routing (row counts) and the routed experts' x panels come from the
+    // top-k kernel: this warp alone waits for it; the other roles wait on the
+    // task queue. The next kernel may start launching now: it waits for this
+    // grid before it reads anything this grid writes, and may read the top-k
+    // kernel's tables at once (that grid is complete).
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+
+    // ---- the step's units (pack_unit) from the per-expert row counts: lane l
+    // owns the run of experts l R .. l R + R - 1 (R = ceil(E / 32)); one warp
+    // exclusive scan of (rows << 16 | active experts) over the runs gives
+    // each active expert its unit index (after the shared expert's 0) and
+    // first row
+    int units;
+    {
+      const int R = (p.E + 31) >> 5;
+      const int e0 = lane * R;
+      int n[kMaxExperts / 32];
+      uint32_t mine = 0;
+      bool bad = false;
+#pragma unroll
+      for (int r = 0; r < kMaxExperts / 32; ++r) {
+        n[r] = r < R && e0 + r < p.E ? __ldcg(p.cnt + e0 + r) : 0;
+        if (n[r] < 0 || n[r] > kMaxTokens) {
+          bad = true;
+          n[r] = 0;
+        }
+        mine += (static_cast<uint32_t>(n[r]) << 16) | (n[r] > 0 ? 1u : 0u);
+      }
+      uint32_t incl = mine;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+      const int routed = static_cast<int>(total & 0xffffu);
+      units = routed + 1;
+      if (__any_sync(0xffffffffu, bad) || units > p.units_max ||
+          static_cast<int>(total >> 16) > p.M * p.K) {
+        if (lane == 0) atomicOr(p.err, kErrBounds);
+        units = 0;
+      } else {
+        const uint32_t excl = incl - mine;
+        int u = 1 + static_cast<int>(excl & 0xffffu), first = static_cast<int>(excl >> 16);
+#pragma unroll
+        for (int r = 0; r < kMaxExperts / 32; ++r) {
+          if (n[r] > 0) {
+            unit_s[u++] = pack_unit(e0 + r, n[r], first);
+            first += n[r];
+          }
+        }
+        if (lane == 0) unit_s[0] = pack_unit(p.E, p.M, p.M * p.K);
+      }
+      __syncwarp();
+      if (blockIdx.x == 0) {  // the table for diagnostics: routed units, then the shared one
+        for (int i = lane; i < units; i += 32) {
+          const uint32_t v = unit_s[i];
+          p.act[i > 0 ? i - 1 : units - 1] =
+              ActiveExpert{static_cast<int>(v & 1023u), static_cast<int>(v >> 16),
+                           static_cast<int>((v >> 10) & 63u), 0};
+        }
+        if (lane == 0) {
+          p.counters[kCtrUnits] = units;
+          p.counters[kCtrRouted] = units > 0 ? units - 1 : 0;
+        }
+      }
+    }
+    const int n13 = units * p.t13;
+    const int n2 = units * p.t2;
+    const int w2full = n2 > p.split_tiles ? n2 - p.split_tiles : 0;  // the rest go in halves
+    const int ntasks = n13 + w2full + 2 * (n2 - w2full);
+
     // Claims the CTA's tasks, one ahead of the producer: the first is the
     // CTA's index, each later one comes from the counter (offset by the grid)
     // once the producer has taken the previous one. It posts each with its
     // unit's entry, then -- for a w2 task -- waits (device scope) until the
     // unit's w13 tiles are all done and publishes that for the producer, so
     // the check runs while the producer still streams the previous task.
-    if (lane == 0) {
-      const int grid = static_cast<int>(gridDim.x);
+    if (lane == 0 && pre_ok) {
       int task = static_cast<int>(blockIdx.x);
-      for (uint32_t j = 0;; ++j) {
+      uint32_t j = 0;
+      bool ok = true;
+      if (pre) {  // task b is posted: claim the next once the producer has taken it
+        j = 1;
+        ok = wait_seq(&misc->prod_seq, 0, abort);
+        task = grid + atomicAdd(p.task_ctr, 1);
+      }
+      for (; ok; ++j) {
         Task k = {0, 0, 0, 0, 0, 0};
         int4 a = make_int4(0, 0, 0, 0);
         for (; task < ntasks; task = grid + atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
@@ -693,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           if (task_valid(a, p)) break;
         }
         const bool last = task >= ntasks;
-        if (!post_task(bars, misc, j, last ? -1 : task, a, abort) || last) break;
+        if (!post_task(bars, misc, j, last ? -1 : task, a, pack_task(k), abort) || last) break;
         if (k.phase == 1 && !wait_ready(p.ready + k.u, p.t13, abort)) break;
         st_release_cta(&misc->ready_seq, static_cast<int>(j));
         if (!wait_seq(&misc->prod_seq, static_cast<int>(j), abort)) break;
