@@ -273,6 +273,31 @@ int moe_route_static(const void* normed, const void* gate_w, const float* bias, 
                      int hidden, int experts, int topk, int32_t* topk_ids, float* topk_w,
                      void* stream);
 
+/*
+ * Attention-seam MXFP8 ("vllm.models.deepseek_v41.amd.mono.layer", store_x8:
+ * the attention seam's fp32 norm output -> the attention's input quant).
+ *
+ * For M bf16 rows x [M, hidden] (device) and the attention norm weight
+ * norm_w bf16 [hidden] (device): ys = x * (mean(x^2) + eps)^(-1/2) * norm_w
+ * computed in fp32 (the sum of squares in the FFN seam's fixed order), then
+ * per 32 columns the E8M0 code of the fp32 values' amax (the same code as the
+ * FFN seam: clamp(ceil(log2(fp32(amax / 448))) + 127, 0, 254), amax floored
+ * at FLT_MIN) into x8_codes u8 [M, hidden/32], and the E4M3 bytes (round to
+ * nearest even) of clamp(ys * 2^(127 - code), -448, 448) into x8 u8
+ * [M, hidden]. Unlike moe_decode_step's seam, the quant reads the fp32 norm
+ * outputs, not their bf16 rounding. If ys is not null the fp32 norm outputs
+ * also go to ys f32 [M, hidden] (device).
+ *
+ * The caller owns every buffer; nothing is allocated and nothing synchronises:
+ * one kernel is enqueued on `stream` (void* holding a cudaStream_t; capture
+ * safe). Limits: 1 <= M <= 48; hidden a multiple of 32 in [32, 8192].
+ * Errors: MOE_ERR_ARG (a null required pointer, eps < 0 or NaN), MOE_ERR_ALIGN
+ * (x, norm_w, x8 or ys not 16-byte aligned), MOE_ERR_RANGE (M),
+ * MOE_ERR_UNSUPPORTED (hidden), MOE_ERR_CUDA (the launch failed).
+ */
+int moe_attn_seam_x8(const void* x, const void* norm_w, int M, int hidden, float eps,
+                     uint8_t* x8, uint8_t* x8_codes, float* ys, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
     L.moe_strerror.restype = ctypes.c_char_p
     L.moe_destroy.argtypes = [vp]
     L.moe_destroy.restype = None
+    L.moe_attn_seam_x8.argtypes = [vp, vp, ip, ip, ctypes.c_float, vp, vp, vp, vp]
+    L.moe_attn_seam_x8.restype = ip
     _LIB = L
     return L
 

@@ -48,6 +48,44 @@ class _DeviceBytes:
                                          "data": (ptr, False), "version": 3}
 
 
+def attn_seam_x8(x: torch.Tensor, norm_w: torch.Tensor, eps: float = 1e-6,
+                 x8: torch.Tensor | None = None, codes: torch.Tensor | None = None,
+                 ys: torch.Tensor | None = None):
+    """Attention-seam MXFP8 of bf16 rows x [M, H] (``moe_attn_seam_x8``): the
+    fp32 RMSNorm with ``norm_w`` bf16 [H], quantised from its fp32 values.
+
+    Returns (x8 uint8 [M, H], codes uint8 [M, H/32], ys) where ys is the fp32
+    norm output [M, H] if a tensor was passed for it, else None. Outputs not
+    passed are allocated here (on x's device); the kernel runs on the current
+    stream.
+    """
+    if x.dim() != 2 or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA bf16 [M, H] tensor")
+    M, H = x.shape
+    if (norm_w.shape != (H,) or norm_w.dtype != torch.bfloat16 or norm_w.device != x.device
+            or not norm_w.is_contiguous()):
+        raise ValueError("norm_w must be a contiguous bf16 [H] tensor on x's device")
+    if H % 32:
+        raise ValueError("H must be a multiple of 32")
+    want = {"x8": ((M, H), torch.uint8), "codes": ((M, H // 32), torch.uint8),
+            "ys": ((M, H), torch.float32)}
+    got = {"x8": x8, "codes": codes, "ys": ys}
+    for k, t in got.items():
+        if t is not None and (tuple(t.shape) != want[k][0] or t.dtype != want[k][1]
+                              or t.device != x.device or not t.is_contiguous()):
+            raise ValueError(f"{k} must be a contiguous {want[k][1]} {want[k][0]} tensor on x's device")
+    if x8 is None:
+        x8 = torch.empty((M, H), dtype=torch.uint8, device=x.device)
+    if codes is None:
+        codes = torch.empty((M, H // 32), dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        stream = torch.cuda.current_stream().cuda_stream
+    check(_lib.lib().moe_attn_seam_x8(
+        x.data_ptr(), norm_w.data_ptr(), M, H, float(eps), x8.data_ptr(), codes.data_ptr(),
+        ys.data_ptr() if ys is not None else None, stream), "moe_attn_seam_x8")
+    return x8, codes, ys
+
+
 def kernel_names() -> list[str]:
     L = _lib.lib()
     return [L.moe_kernel_name(i).decode() for i in range(L.moe_kernel_count())]

@@ -10,7 +10,8 @@ consumer):
 * small tensors on the host with numpy's PCG64, one stream per tensor and
   per token row, so a row can be redrawn alone:
   - x: bf16(N(0, 1)) [M, H], row t attempt a from stream (seed, 1, t, a);
-  - norm weight: bf16(1 + N(0, 0.1)) [H];
+  - norm weight: bf16(1 + N(0, 0.1)) [H] (the attention seam's norm
+    weight the same, from its own stream);
   - gate weight: bf16(N(0, 0.02)) [E, H];
   - bias f32 [E]: N(0, 0.01), U(-0.01, 0.01), or Zipf(s = 1.2) on a seeded
     permutation of the experts, bias[perm[r]] = C * (r + 1)^-1.2;
@@ -73,6 +74,10 @@ class Workload:
 
 
 FULL = MoeDims(hidden=5120, experts=256, topk=8, inter=2048, shared_inter=2048)
+# The runner page's layer has 384 routed experts over the same hidden size
+# (gate_w [384, 5120]); its top-k and unsharded intermediate are not printed:
+# these take k = 8 and I = 2048 as above, with E4M3 routed weights.
+E384 = MoeDims(hidden=5120, experts=384, topk=8, inter=2048, shared_inter=2048)
 
 WORKLOADS = {
     w.name: w
@@ -89,10 +94,14 @@ WORKLOADS = {
                  "max step width M=48, uniform bias"),
         Workload("full_m48_zipf", FULL, 48, 4, "zipf",
                  "max step width M=48, Zipf(1.2) bias on ~32 hot experts"),
+        Workload("full_e384_m1", E384, 1, 5, "uniform",
+                 "384-expert layer, single-token decode, M=1, H5120 E384 k8 I2048"),
+        Workload("full_e384_m48", E384, 48, 6, "uniform",
+                 "384-expert layer, M=48, uniform bias"),
     ]
 }
 
-_TAG_X, _TAG_NORM, _TAG_GATE, _TAG_BIAS, _TAG_PERM = 1, 2, 3, 4, 5
+_TAG_X, _TAG_NORM, _TAG_GATE, _TAG_BIAS, _TAG_PERM, _TAG_ATTN_NORM = 1, 2, 3, 4, 5, 6
 _T_W13, _T_W2, _T_SW13, _T_SW2 = 11, 12, 13, 14
 
 
@@ -117,6 +126,12 @@ def token_rows(wl: Workload, attempts=None, m: int | None = None) -> torch.Tenso
     if m == 0:
         return torch.zeros(0, wl.dims.hidden, dtype=torch.bfloat16)
     return torch.cat([token_row(wl, t, attempts[t]) for t in range(m)])
+
+
+def attn_norm_weight(wl: Workload) -> torch.Tensor:
+    """The attention seam's norm weight, bf16(1 + N(0, 0.1)) [H] on the host
+    (its own stream; drawn like the FFN norm weight)."""
+    return _bf16(1.0 + 0.1 * _rng(wl.seed, _TAG_ATTN_NORM).standard_normal(wl.dims.hidden))
 
 
 def router_inputs(wl: Workload) -> dict:

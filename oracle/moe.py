@@ -29,6 +29,12 @@ Steps and the passages they follow:
 5. ``combine`` -- out = bf16(sum_j w_j * y_{id_j} + y_shared) (``out [M, HIDDEN]
    bf16``, ``DSV41MonoLayer._outs``, runner page). The residual is not added.
 
+Outside the FFN step, the attention seam's input quant (``store_x8``, layer
+page: "the attention seam's norm output ... -> vLLM's MXFP8 of each 32"):
+``attn_norm`` is the same norm with the attention norm weight, not rounded
+(``seam.stage_norm``'s outputs are f32), and ``attn_seam_quant`` quantises
+those fp32 values in 32-groups with the same code and E4M3 rule.
+
 Pins (tests/test_oracle_moe.py): hand-worked RMSNorm values
 (tests/golden/rmsnorm_cases.txt), silu closed forms, brute-force top-k over
 all k-subsets on small E, an expert built from hand-chosen bytes and codes
@@ -62,6 +68,28 @@ def rmsnorm(x, w, eps: float = 1e-6):
 def seam_quant(normed):
     """MXFP8 of the bf16 normed rows: (x8 bytes [M, H], codes [M, H/32])."""
     return quant_rows(normed)
+
+
+def attn_norm(x, w, eps: float = 1e-6):
+    """The attention seam's norm output x * (mean_h(x^2) + eps)^(-1/2) * w in
+    float64, not rounded (the GPU's fp32 values are compared to it within the
+    fp32 error bound; its MXFP8 is taken on the GPU's own fp32 values).
+
+    x: float64 [M, H] (bf16 values), w: float64 [H] (bf16 values).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return x * r * w
+
+
+def attn_seam_quant(ys):
+    """MXFP8 of fp32 norm outputs (fp32-exact float64 [M, H]) in 32-groups:
+    (x8 bytes [M, H], codes [M, H/32]) -- ``store_x8`` on the attention seam."""
+    ys = np.asarray(ys, dtype=np.float64)
+    if not np.array_equal(fp32_rn(ys), ys):
+        raise ValueError("attn_seam_quant: the inputs must be fp32 values")
+    return quant_rows(ys)
 
 
 def sigmoid(z):

@@ -88,3 +88,19 @@ def test_step_rejects_null_handle_and_range(L):
     assert L.moe_scratch_bytes(None) == 0
     L.moe_destroy(None)
     assert MOE_ERR_RANGE == -2
+
+
+def test_attn_seam_argument_checks_without_a_gpu(L):
+    f = L.moe_attn_seam_x8
+    x, w, b, c, y = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    assert f(None, w, 4, 256, 1e-6, b, c, y, None) == MOE_ERR_ARG
+    assert f(x, w, 4, 256, 1e-6, b, None, y, None) == MOE_ERR_ARG
+    assert f(x + 8, w, 4, 256, 1e-6, b, c, y, None) == MOE_ERR_ALIGN
+    assert f(x, w, 4, 256, 1e-6, b + 4, c, y, None) == MOE_ERR_ALIGN
+    assert f(x, w, 4, 256, 1e-6, b, c, y + 4, None) == MOE_ERR_ALIGN
+    assert f(x, w, 0, 256, 1e-6, b, c, y, None) == MOE_ERR_RANGE
+    assert f(x, w, 49, 256, 1e-6, b, c, y, None) == MOE_ERR_RANGE
+    for h in (0, 16, 1000, 8224):
+        assert f(x, w, 4, h, 1e-6, b, c, y, None) == MOE_ERR_UNSUPPORTED, h
+    assert f(x, w, 4, 256, -1.0, b, c, y, None) == MOE_ERR_ARG
+    assert f(x, w, 4, 256, float("nan"), b, c, y, None) == MOE_ERR_ARG

@@ -12,6 +12,7 @@ import math
 import os
 
 import numpy as np
+import pytest
 
 from oracle import moe
 from oracle.mx import dequant_rows, quant_rows
@@ -38,6 +39,51 @@ def test_rmsnorm_hand_cases():
     for x, w, eps, want in cases:
         got = moe.rmsnorm(x[None, :], w, eps)[0]
         assert np.array_equal(got, want), (x, w, got, want)
+
+
+def test_attn_norm_closed_forms_and_ffn_rounding():
+    # a constant row c: mean(x^2) = c^2, so y = c w / sqrt(c^2 + eps)
+    w = np.linspace(0.5, 1.5, 64)
+    y = moe.attn_norm(np.full((1, 64), 2.0), w, 0.0)[0]
+    assert np.array_equal(y, w)
+    y = moe.attn_norm(np.full((1, 64), -3.0), w, 1e-6)[0]
+    assert np.allclose(y, -3.0 * w / math.sqrt(9.0 + 1e-6), rtol=1e-15, atol=0)
+    # alternating +-a with unit weight: +-a / sqrt(a^2 + eps)
+    x = np.tile([0.5, -0.5], 32)[None, :]
+    y = moe.attn_norm(x, np.ones(64), 1e-6)[0]
+    assert np.allclose(y, x[0] / math.sqrt(0.25 + 1e-6), rtol=1e-15, atol=0)
+    # the FFN seam's norm is its bf16 rounding (hand-worked bf16 values)
+    for x, w, eps, want in _rms_cases():
+        got = moe.bf16_rne(moe.attn_norm(x[None, :], w, eps))[0]
+        assert np.array_equal(got, want), (x, got, want)
+
+
+def test_attn_seam_quant_hand_case():
+    """fp32 values that bf16 cannot hold, quantised by hand (E4M3: bias 7,
+    3 mantissa bits, subnormals k * 2^-9; codes from ceil(log2(amax / 448)))."""
+    v = np.zeros(128)
+    # group 0: amax 448 -> code 127, multiplier 1
+    v[0:7] = [448.0, 1.0625, 1.0625 + 2.0 ** -20, 1.0 + 2.0 ** -20, -0.0, 2.0 ** -10,
+              3.0 * 2.0 ** -10]
+    # group 1: amax 897 -> 897 / 448 = 2.0022 -> code 129, multiplier 1/4
+    v[32:35] = [897.0, 896.0, -1.0]
+    # group 2: all zero -> code 0
+    # group 3: amax 448 (1 + 2^-20) (bf16 would round it to 448, code 127) -> code 128
+    v[96:98] = [448.0 * (1.0 + 2.0 ** -20), 1.0]
+    b, c = moe.attn_seam_quant(v[None, :])
+    assert list(c[0]) == [127, 129, 0, 128]
+    want = np.zeros(128, dtype=np.uint8)
+    # 448 = 1.75 * 2^8 -> 0 1111 110; 1.0625 ties 1.0 / 1.125 -> even 1.0 (0x38);
+    # just above the tie -> 1.125 (0x39); 1 + 2^-20 -> 1.0; -0.0 keeps its sign;
+    # 2^-10 ties 0 / 2^-9 -> 0; 1.5 * 2^-9 ties 2^-9 / 2^-8 -> 2^-8 (0x02)
+    want[0:7] = [0x7E, 0x38, 0x39, 0x38, 0x80, 0x00, 0x02]
+    # 897/4 = 224.25 -> 224 = 1.75 * 2^7 (0 1110 110); 896/4 = 224; -1/4 = -(0 0101 000)
+    want[32:35] = [0x76, 0x76, 0xA8]
+    # 448 (1 + 2^-20) / 2 -> 224; 1/2 = 2^-1 -> 0 0110 000
+    want[96:98] = [0x76, 0x30]
+    assert np.array_equal(b[0], want), [hex(x) for x in b[0][:8]]
+    with pytest.raises(ValueError):
+        moe.attn_seam_quant(np.full((1, 32), 0.1))  # 0.1 is not an fp32 value
 
 
 def test_silu_sigmoid_closed_forms():
