@@ -34,6 +34,9 @@ sys.path.insert(0, ROOT)
 METRIC = "µs per MoE decode step and achieved HBM GB/s (% of 8 TB/s) at M=1..48"
 DEFAULT_WORKLOAD = "full_m48_uniform"
 SWEEP = ["full_m48_zipf", "full_m1", "full_m16", "small_m4"]
+# beyond the step at M = 1..48 of the 256-expert layer: the 384-expert layer
+# and the attention seam's MXFP8 (reported under "next_rows")
+NEXT_ROWS = ["full_e384_m1", "full_e384_m48"]
 
 
 def parse_args():
@@ -182,6 +185,36 @@ def capture(layer, x, dev, events=None):
     torch.cuda.synchronize(dev)
     layer.set_timing_events(None)
     return g, out
+
+
+def time_attn_seam(wl, dev, flush, steps: int) -> dict:
+    """moe_attn_seam_x8 on the workload's M rows: CUDA events around each
+    launch, L2 flushed before each; bytes = x, weight, E4M3 bytes and codes."""
+    from mxfp8_moe_decode_gb300 import attn_seam_x8
+    from mxfp8_moe_decode_gb300 import workloads as W
+    x = W.token_rows(wl).to(dev)
+    w = W.attn_norm_weight(wl).to(dev)
+    M, H = x.shape
+    x8 = torch.empty((M, H), dtype=torch.uint8, device=dev)
+    codes = torch.empty((M, H // 32), dtype=torch.uint8, device=dev)
+    cur = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        attn_seam_x8(x, w, wl.dims.eps, x8=x8, codes=codes)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for e0, e1 in ev:
+        flush.fill_(1)
+        e0.record(cur)
+        attn_seam_x8(x, w, wl.dims.eps, x8=x8, codes=codes)
+        e1.record(cur)
+    torch.cuda.synchronize(dev)
+    us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+    nbytes = M * H * 2 + H * 2 + M * H + M * H // 32
+    return {"M": M, "hidden": H, "us_per_call": round(us, 3), "bytes": nbytes,
+            "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "note": "one launch per row block, latency-bound (bytes << what HBM moves in "
+                    "a launch's latency); L2 flushed before each timed launch"}
 
 
 def time_layer(layer, x, dev, steps: int, warmup: int, flush):
@@ -345,13 +378,13 @@ def run_gpu(args):
         e2e.append(e0.elapsed_time(e1))
     e2e_us = statistics.mean(e2e) * 1e3
 
-    sweep = {}
+    sweep, next_rows = {}, {}
     if not args.no_sweep and world == 1:
         layer.close()
         del layer, graph
         torch.cuda.empty_cache()
         prev_seed, prev_ew = wl.seed, ew
-        for name in SWEEP:
+        for name in SWEEP + NEXT_ROWS:
             swl = W.WORKLOADS[name]
             reuse = prev_ew if (swl.seed == prev_seed and swl.dims == d) else None
             if reuse is None:
@@ -363,7 +396,8 @@ def run_gpu(args):
             us2 = statistics.mean(ms) * 1e3
             a2 = W.algorithmic_bytes(swl.dims, u2)
             e2 = (u2 + 1) * swl.dims.expert_bytes()
-            sweep[name] = {"M": swl.tokens, "us_per_step": round(us2, 2),
+            (sweep if name in SWEEP else next_rows)[name] = {
+                           "M": swl.tokens, "experts": swl.dims.experts, "us_per_step": round(us2, 2),
                            "replay_us_per_step": round(statistics.mean(rms) * 1e3, 2),
                            "unique_routed": u2, "alg_bytes": a2,
                            "step_gbs": round(a2 / (us2 * 1e-6) / 1e9, 1),
@@ -374,6 +408,10 @@ def run_gpu(args):
             L2.close()
             del L2
             prev_seed, prev_ew = swl.seed, ew2
+        del prev_ew
+        torch.cuda.empty_cache()
+        next_rows["attn_seam_x8"] = time_attn_seam(W.WORKLOADS[DEFAULT_WORKLOAD], dev, flush,
+                                                   max(10, args.steps // 2))
 
     line = {
         "metric": METRIC,
@@ -411,6 +449,8 @@ def run_gpu(args):
     }
     if sweep:
         line["sweep"] = sweep
+    if next_rows:
+        line["next_rows"] = next_rows
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_experts, unique)
     if world > 1:

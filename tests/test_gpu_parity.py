@@ -180,7 +180,9 @@ def test_small_m4():
 
 @pytest.mark.parametrize("name,sample", [("full_m1", None), ("full_m16", [0, 7, 15]),
                                          ("full_m48_uniform", [0, 23, 47]),
-                                         ("full_m48_zipf", [0, 23, 47])])
+                                         ("full_m48_zipf", [0, 23, 47]),
+                                         ("full_e384_m1", None),
+                                         ("full_e384_m48", [0, 23, 47])])
 def test_full_size(name, sample):
     L = Layer(W.WORKLOADS[name])
     try:
