@@ -190,6 +190,8 @@ def capture(layer, x, dev, events=None):
 def time_attn_seam(wl, dev, flush, steps: int) -> dict:
     """moe_attn_seam_x8 on the workload's M rows: CUDA events around each
     launch, L2 flushed before each; bytes = x, weight, E4M3 bytes and codes."""
+    import torch
+
     from mxfp8_moe_decode_gb300 import attn_seam_x8
     from mxfp8_moe_decode_gb300 import workloads as W
     x = W.token_rows(wl).to(dev)
@@ -204,7 +206,7 @@ def time_attn_seam(wl, dev, flush, steps: int) -> dict:
           for _ in range(steps)]
     torch.cuda.synchronize(dev)
     for e0, e1 in ev:
-        flush.fill_(1)
+        flush()
         e0.record(cur)
         attn_seam_x8(x, w, wl.dims.eps, x8=x8, codes=codes)
         e1.record(cur)
@@ -213,7 +215,7 @@ def time_attn_seam(wl, dev, flush, steps: int) -> dict:
     nbytes = M * H * 2 + H * 2 + M * H + M * H // 32
     return {"M": M, "hidden": H, "us_per_call": round(us, 3), "bytes": nbytes,
             "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-            "note": "one launch per row block, latency-bound (bytes << what HBM moves in "
+            "note": "one CTA per token row, latency-bound (bytes << what HBM moves in "
                     "a launch's latency); L2 flushed before each timed launch"}
 
 
