@@ -18,8 +18,9 @@ E8M0 inputs. Every function cites the passage of the source pages it follows:
 
 Modules:
 
-* :mod:`oracle.numerics` -- bf16 / fp32 rounding and the OCP E4M3 codec.
-* :mod:`oracle.mx`       -- the E8M0 scale code and 32-group quantisation.
+* :mod:`oracle.numerics` -- bf16 / fp32 rounding and the OCP E4M3 and E2M1 codecs.
+* :mod:`oracle.mx`       -- the E8M0 scale code, 32-group quantisation, and
+  the dequantisation of 32 x 32-block E4M3 and per-row 1 x 32 E2M1 weights.
 * :mod:`oracle.moe`      -- RMSNorm, router, experts, combine, whole step.
 
 Pinning status (what fixes each function other than itself) is listed in each

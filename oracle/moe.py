@@ -50,7 +50,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from .mx import dequant_rows, dequant_weight, quant_rows
+from .mx import dequant_fp4_rows, dequant_rows, dequant_weight, quant_rows
 from .numerics import bf16_rne, fp32_rn
 
 
@@ -151,6 +151,12 @@ class ExpertWeights:
     @staticmethod
     def from_quantised(w13_b, w13_s, w2_b, w2_s) -> "ExpertWeights":
         return ExpertWeights(w13=dequant_weight(w13_b, w13_s), w2=dequant_weight(w2_b, w2_s))
+
+    @staticmethod
+    def from_fp4(w13_p, w13_s, w2_p, w2_s) -> "ExpertWeights":
+        """MXFP4 routed expert (runner page: ``w13 [E, 2 inter, 2560] fp4x2``,
+        ``w2 [E, 5120, inter / 2] fp4x2``, scales per row per 32 columns)."""
+        return ExpertWeights(w13=dequant_fp4_rows(w13_p, w13_s), w2=dequant_fp4_rows(w2_p, w2_s))
 
 
 def expert(x_hat, ew: ExpertWeights):

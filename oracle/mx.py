@@ -18,6 +18,11 @@ Source passages:
 * ``MonoLayerWeights.check`` / ``AttnWeights.check`` (runner page): a weight
   [R, C] e4m3 has a [R/32, C/32] uint8 E8M0 scale, one code per 32 x 32 block
   (e.g. wqkv [1792, 5120] with a [56, 160] scale).
+* ``MonoLayerWeights`` (runner page): the routed w13 / w2 are
+  ``float4_e2m1fn_x2`` ([E, 2 inter, 2560] for 5120 columns) with scales of
+  HIDDEN // 32 columns per weight row (``w13_s [E * 2 inter, HIDDEN // 32]``):
+  one code per row per 32 columns (``dequant_fp4_rows``). The pages store
+  them in AITER's shuffled orders; the plain row-major order is taken here.
 
 Readings (where the pages leave a step open):
 
@@ -34,14 +39,16 @@ Pins (tests/test_oracle_mx.py): hand cases (448 -> 127, 448 * 2^k -> 127 + k,
 just above -> 128 + k, 0 -> 0), every positive finite bf16 amax against the
 exact rational ceil(log2(amax / 448)) via ``fractions.Fraction``, the
 [1792, 5120] -> [56, 160] scale shape, a one-element block round trip, and the
-golden cases in tests/golden/mx_code_cases.txt.
+golden cases in tests/golden/mx_code_cases.txt; ``dequant_fp4_rows`` by an
+independent element loop with per-row codes (E2M1 itself is pinned in
+tests/test_oracle_numerics.py against tests/golden/e2m1_values.txt).
 """
 
 from __future__ import annotations
 
 import numpy as np
 
-from .numerics import E4M3_MAX, e4m3_decode, e4m3_encode_rne
+from .numerics import E4M3_MAX, e2m1_decode, e4m3_decode, e4m3_encode_rne, unpack_fp4x2
 
 FLT_MIN = 2.0 ** -126
 GROUP = 32
@@ -118,3 +125,18 @@ def dequant_weight(b, code):
     s = mx_scale(code)
     s = np.repeat(np.repeat(s, GROUP, axis=0), GROUP, axis=1)
     return e4m3_decode(b) * s
+
+
+def dequant_fp4_rows(packed, code):
+    """MXFP4 weight: E2M1 pairs [R, C/2] (``unpack_fp4x2`` order) with one code
+    per row per 32 columns [R, C/32] -> float64 [R, C].
+
+    Element (r, c) is scaled by code (r, c // 32): the runner page's routed
+    w13 / w2 carry their scales per row ("per-row 1 x 32": ``w13_s`` has
+    HIDDEN // 32 columns per weight row).
+    """
+    vals = e2m1_decode(unpack_fp4x2(packed))
+    code = np.asarray(code)
+    if code.shape != (vals.shape[0], vals.shape[1] // GROUP) or vals.shape[1] % GROUP:
+        raise ValueError(f"dequant_fp4_rows: scale {code.shape} does not match {vals.shape}")
+    return vals * np.repeat(mx_scale(code), GROUP, axis=1)

@@ -17,6 +17,12 @@ TEST INFRASTRUCTURE ONLY (see the package header).
   the method clamps before it converts (``clamp_fp8`` in ``store_x8``, layer
   page).
 
+* E2M1 (OCP MX FP4): 1 sign bit, 2 exponent bits with bias 1, 1 mantissa
+  bit; exponent field 0 is subnormal (m/2); no infinity or NaN; values 0,
+  0.5, 1, 1.5, 2, 3, 4, 6 and their negatives. The runner page's routed
+  weights are ``torch.float4_e2m1fn_x2`` (two per byte): element 2j sits in
+  the low nibble of byte j (``unpack_fp4x2``).
+
 Pins (tests/test_oracle_numerics.py): all 256 decoded values against torch's
 float8_e4m3fn and hand values from the OCP definition; every representable
 value encodes to itself; every midpoint goes to the even neighbour and one
@@ -118,3 +124,34 @@ def e4m3_encode_rne(v):
     code = np.where(exact, hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
     sign = np.signbit(v).astype(np.uint8) << 7
     return (code | sign).astype(np.uint8)
+
+
+def _e2m1_value(nibble: int) -> float:
+    """Value of one E2M1 code (4 bits) from the OCP MX FP4 definition."""
+    s = -1.0 if nibble & 0x8 else 1.0
+    exp = (nibble >> 1) & 0x3
+    man = nibble & 0x1
+    if exp == 0:
+        return s * (man / 2.0)
+    return s * (1.0 + man / 2.0) * 2.0 ** (exp - 1)
+
+
+E2M1_VALUES = np.array([_e2m1_value(n) for n in range(16)], dtype=np.float64)
+
+
+def unpack_fp4x2(packed):
+    """uint8 [..., C/2] holding two E2M1 codes per byte -> codes uint8 [..., C]
+    (element 2j = the low nibble of byte j, element 2j + 1 = the high nibble)."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 0x0F
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def e2m1_decode(codes):
+    """E2M1 codes (uint8 values 0..15) -> float64 values."""
+    c = np.asarray(codes, dtype=np.uint8)
+    if np.any(c > 15):
+        raise ValueError("e2m1_decode: codes are 4-bit")
+    return E2M1_VALUES[c]

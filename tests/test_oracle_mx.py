@@ -136,3 +136,24 @@ def test_dequant_weight_block_addressing():
     with pytest.raises(ValueError):
         dequant_weight(w, codes[:2])
     assert e4m3_decode(np.uint8(0xC0)) == -2.0
+
+
+def test_dequant_fp4_rows_per_row_scales():
+    """Each row's 32-column block has its own code (1 x 32 scales): an
+    independent element loop over a hand-set pattern."""
+    from oracle.mx import dequant_fp4_rows
+    R, C = 3, 64
+    rng = np.random.default_rng(5)
+    packed = rng.integers(0, 256, size=(R, C // 2), dtype=np.uint8)
+    code = np.array([[127, 130], [120, 127], [0, 254]], dtype=np.uint8)
+    got = dequant_fp4_rows(packed, code)
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for r in range(R):
+        for c in range(C):
+            byte = int(packed[r, c // 2])
+            nib = byte & 0xF if c % 2 == 0 else byte >> 4
+            v = table[nib & 7] * (-1.0 if nib & 8 else 1.0)
+            want = v * 2.0 ** (int(code[r, c // 32]) - 127)
+            assert got[r, c] == want, (r, c, got[r, c], want)
+    with pytest.raises(ValueError):
+        dequant_fp4_rows(packed, code[:, :1])

@@ -13,7 +13,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.numerics import (E4M3_VALUES, bf16_rne, e4m3_decode, e4m3_encode_rne)
+from oracle.numerics import (E4M3_VALUES, bf16_rne, e2m1_decode, e4m3_decode, e4m3_encode_rne,
+                             unpack_fp4x2)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -117,3 +118,26 @@ def test_bf16_rne_hand_ties():
     assert bf16_rne(-(1 + 2.0 ** -8 + 2.0 ** -30)) == -(1 + 2.0 ** -7)
     assert bf16_rne(2.0 ** -133) == 2.0 ** -133  # smallest bf16 subnormal
     assert bf16_rne(2.0 ** -134) == 0.0  # tie with zero -> even (zero)
+
+
+def test_e2m1_hand_values():
+    rows = []
+    with open(os.path.join(GOLDEN, "e2m1_values.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                p = line.split()
+                rows.append((int(p[0], 16), float(p[4])))
+    assert [c for c, _ in rows] == list(range(16))
+    got = e2m1_decode(np.arange(16, dtype=np.uint8))
+    for c, v in rows:
+        assert got[c] == v and math.copysign(1.0, got[c]) == math.copysign(1.0, v), (c, got[c], v)
+    with pytest.raises(ValueError):
+        e2m1_decode(np.uint8(16))
+
+
+def test_fp4x2_nibble_order():
+    # byte j holds element 2j in its low nibble and 2j + 1 in its high nibble
+    p = np.array([[0x21, 0xF7, 0x80]], dtype=np.uint8)
+    assert unpack_fp4x2(p).tolist() == [[0x1, 0x2, 0x7, 0xF, 0x0, 0x8]]
+    assert e2m1_decode(unpack_fp4x2(p)).tolist() == [[0.5, 1.0, 6.0, -6.0, 0.0, -0.0]]
