@@ -36,7 +36,7 @@ DEFAULT_WORKLOAD = "full_m48_uniform"
 SWEEP = ["full_m48_zipf", "full_m1", "full_m16", "small_m4"]
 # beyond the step at M = 1..48 of the 256-expert layer: the 384-expert layer
 # and the attention seam's MXFP8 (reported under "next_rows")
-NEXT_ROWS = ["full_e384_m1", "full_e384_m48"]
+NEXT_ROWS = ["full_e384_m1", "full_e384_m48", "full_e384_fp4_m1", "full_e384_fp4_m48"]
 
 
 def parse_args():
@@ -161,7 +161,7 @@ def make_layer(wl, dev, ew=None):
     weights = {"norm_w": ri["norm_w"].to(dev), "gate_w": ri["gate_w"].to(dev),
                "bias": ri["bias"].to(dev), **ew}
     layer = MoeDecode(d.hidden, d.experts, d.topk, d.inter, weights, max_tokens=d.max_tokens,
-                      eps=d.eps)
+                      eps=d.eps, routed=d.routed)
     x = W.token_rows(wl).to(dev)
     torch.cuda.synchronize(dev)
     return layer, x, ew
@@ -347,7 +347,7 @@ def run_gpu(args):
     alg = W.algorithmic_bytes(d, unique)
     ix = names.index("experts")
     # the expert kernel streams every touched expert (w13 + w2 + their scales) once
-    exp_bytes = (unique + 1) * d.expert_bytes()
+    exp_bytes = unique * d.expert_bytes() + d.shared_bytes()
     ach = exp_bytes / (kmean[ix] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": "experts", "achieved": round(ach, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
@@ -397,7 +397,7 @@ def run_gpu(args):
             del g2
             us2 = statistics.mean(ms) * 1e3
             a2 = W.algorithmic_bytes(swl.dims, u2)
-            e2 = (u2 + 1) * swl.dims.expert_bytes()
+            e2 = u2 * swl.dims.expert_bytes() + swl.dims.shared_bytes()
             (sweep if name in SWEEP else next_rows)[name] = {
                            "M": swl.tokens, "experts": swl.dims.experts, "us_per_step": round(us2, 2),
                            "replay_us_per_step": round(statistics.mean(rms) * 1e3, 2),

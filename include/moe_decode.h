@@ -66,7 +66,16 @@ extern "C" {
  *  shared_inter  the shared expert's intermediate size; must equal inter.
  *  max_tokens    largest M a step may use, 1..48 (the pages' MAX_TOKENS).
  *  eps           RMSNorm epsilon (1e-6 for the pages' layer).
+ *  routed_format MOE_ROUTED_E4M3 (0): routed experts in E4M3 with one E8M0
+ *                code per 32 x 32 block; MOE_ROUTED_E2M1 (1): routed experts
+ *                in MXFP4 ("vllm.models.deepseek_v41.amd.mono.runner",
+ *                MonoLayerWeights: w13 / w2 float4_e2m1fn_x2 with one E8M0
+ *                code per row per 32 columns), read by the tensor cores as
+ *                E2M1 against the E4M3 activations. The shared expert is E4M3
+ *                with 32 x 32 blocks in both.
  */
+#define MOE_ROUTED_E4M3 0
+#define MOE_ROUTED_E2M1 1
 typedef struct moe_config {
   int hidden;
   int experts;
@@ -75,6 +84,7 @@ typedef struct moe_config {
   int shared_inter;
   int max_tokens;
   float eps;
+  int routed_format;
 } moe_config;
 
 /*
@@ -90,6 +100,13 @@ typedef struct moe_config {
  *  w2_s    u8   [E, H/32, I/32]
  *  sw13, sw13_s, sw2, sw2_s              the shared expert, same layouts
  *                                        without the E axis
+ * With routed_format MOE_ROUTED_E2M1 the routed tensors are instead
+ *  w13     e2m1x2 [E, 2I, H/2]           two E2M1 codes per byte, column 2j in
+ *                                        the low nibble of byte j; 32-byte aligned
+ *  w13_s   u8   [E, 2I, H/32]            E8M0 code per row per 32 columns
+ *  w2      e2m1x2 [E, H, I/2]            32-byte aligned
+ *  w2_s    u8   [E, H, I/32]
+ * (the pages store them in AITER's shuffled orders; these are row-major).
  */
 typedef struct moe_weights {
   const void* norm_w;
@@ -206,7 +223,9 @@ int moe_step_launches(const moe_handle* h, int M);
  *      count, and experts no token picked, are unspecified; at M = 1 no
  *      routed panel is written (every unit reads the shared expert's).
  *  MOE_REGION_H8        u8  [units][I / 128][7168] the same layout for the
- *      requantised silu(g) * u rows, by unit (MOE_REGION_ACTIVE order)
+ *      requantised silu(g) * u rows, by the expert kernel's unit index: the
+ *      shared expert first, then the routed experts of MOE_REGION_ACTIVE in
+ *      its order
  *  MOE_REGION_PARTIAL   f32 [rows][H]  expert output rows y
  *  MOE_REGION_ACTIVE    i32 [E + 1][4] active experts: expert, first row, rows, 0
  *  MOE_REGION_TOKPOS    i32 [M][k + 1] row of (token, pick); pick k = shared expert

@@ -28,7 +28,12 @@ REGION_GATHERED, REGION_H8, REGION_PARTIAL, REGION_ACTIVE, REGION_TOKPOS = range
 class MoeConfig(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("experts", ctypes.c_int), ("topk", ctypes.c_int),
                 ("inter", ctypes.c_int), ("shared_inter", ctypes.c_int),
-                ("max_tokens", ctypes.c_int), ("eps", ctypes.c_float)]
+                ("max_tokens", ctypes.c_int), ("eps", ctypes.c_float),
+                ("routed_format", ctypes.c_int)]
+
+
+MOE_ROUTED_E4M3 = 0
+MOE_ROUTED_E2M1 = 1
 
 
 class MoeWeights(ctypes.Structure):

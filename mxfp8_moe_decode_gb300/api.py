@@ -20,11 +20,23 @@ WEIGHT_KEYS = ("norm_w", "gate_w", "bias", "w13", "w13_s", "w2", "w2_s",
 
 
 def _u8(t: torch.Tensor) -> torch.Tensor:
-    return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
+    fp4x2 = getattr(torch, "float4_e2m1fn_x2", None)
+    return t.view(torch.uint8) if t.dtype in (torch.float8_e4m3fn, fp4x2) else t
 
 
-def expected_shapes(hidden: int, experts: int, inter: int, shared_inter: int) -> dict:
+def expected_shapes(hidden: int, experts: int, inter: int, shared_inter: int,
+                    routed: str = "e4m3") -> dict:
+    """Weight shapes and dtypes; ``routed="e2m1"``: MXFP4 routed experts (E2M1
+    pairs, one code per row per 32 columns)."""
     h, e, i, s = hidden, experts, inter, shared_inter
+    if routed == "e2m1":
+        fp4 = {"w13": ((e, 2 * i, h // 2), torch.uint8),
+               "w13_s": ((e, 2 * i, h // 32), torch.uint8),
+               "w2": ((e, h, i // 2), torch.uint8),
+               "w2_s": ((e, h, i // 32), torch.uint8)}
+        return {**expected_shapes(hidden, experts, inter, shared_inter), **fp4}
+    if routed != "e4m3":
+        raise ValueError(f"routed weights: 'e4m3' or 'e2m1', not {routed!r}")
     return {
         "norm_w": ((h,), torch.bfloat16),
         "gate_w": ((e, h), torch.bfloat16),
@@ -95,20 +107,21 @@ class MoeDecode:
     """One MoE layer's decode step on one GPU.
 
     weights: dict with the tensors of ``WEIGHT_KEYS`` on the target device
-    (E4M3 tensors as uint8 or float8_e4m3fn). The handle keeps references to
-    them; they must not change while it lives (the E8M0 scales are packed at
-    creation).
+    (E4M3 tensors as uint8 or float8_e4m3fn; with ``routed="e2m1"`` the routed
+    w13 / w2 as uint8 E2M1 pairs or float4_e2m1fn_x2, their scales per row).
+    The handle keeps references to them; they must not change while it lives
+    (the E8M0 scales are packed at creation).
     """
 
     def __init__(self, hidden: int, experts: int, topk: int, inter: int, weights: dict,
                  shared_inter: int | None = None, max_tokens: int = 48, eps: float = 1e-6,
-                 device=None):
+                 device=None, routed: str = "e4m3"):
         L = _lib.lib()
         shared_inter = inter if shared_inter is None else shared_inter
         dev = torch.device(device) if device is not None else weights["gate_w"].device
         if dev.type != "cuda":
             raise ValueError("MoeDecode needs CUDA tensors")
-        want = expected_shapes(hidden, experts, inter, shared_inter)
+        want = expected_shapes(hidden, experts, inter, shared_inter, routed)
         self._w = {}
         for k, (shape, dtype) in want.items():
             t = weights[k]
@@ -121,7 +134,8 @@ class MoeDecode:
         self.hidden, self.experts, self.topk, self.inter = hidden, experts, topk, inter
         self.max_tokens = max_tokens
         self.device = dev
-        cfg = MoeConfig(hidden, experts, topk, inter, shared_inter, max_tokens, eps)
+        fmt = _lib.MOE_ROUTED_E2M1 if routed == "e2m1" else _lib.MOE_ROUTED_E4M3
+        cfg = MoeConfig(hidden, experts, topk, inter, shared_inter, max_tokens, eps, fmt)
         wt = MoeWeights(*[self._w[k].data_ptr() for k in WEIGHT_KEYS])
         h = ctypes.c_void_p()
         with torch.cuda.device(dev):

@@ -81,32 +81,46 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2D uint8 matrix [rows][cols] (row stride = cols bytes), box = 128 bytes x box_rows,
-// 128-byte swizzle (the layout the MMA's shared-memory descriptors describe).
+// Element type of a weight tensor map: E4M3 bytes, or E2M1 pairs (two 4-bit
+// codes per byte in global memory) that the copy spreads into 16-byte
+// shared-memory units of 16 codes (8 bytes of codes, 8 bytes of gap): the
+// operand form the tensor cores read for an E2M1 matrix, one byte per element
+// of shared memory like E4M3 (so the stage's layout and descriptors are the same).
+struct WeightType {
+  CUtensorMapDataType dt;
+  uint64_t bytes_num, bytes_den;  // global bytes per element = num / den
+};
+constexpr WeightType kE4M3Map = {CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 1};
+constexpr WeightType kE2M1Map = {CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 1, 2};
+
+// 2D matrix [rows][cols] (cols elements per row), box = 128 elements x
+// box_rows, 128-byte swizzle (the layout the MMA's shared-memory descriptors describe).
 bool encode_rows(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
-                 uint32_t box_rows) {
+                 uint32_t box_rows, WeightType wt = kE4M3Map) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols};
+  const cuuint64_t strides[1] = {cols * wt.bytes_num / wt.bytes_den};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK), box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(tm, wt.dt, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3D uint8 tensor [planes][rows][cols] (strides cols and rows * cols bytes),
-// box = 128 bytes x box_rows x box_planes, 128-byte swizzle.
+// 3D tensor [planes][rows][cols], box = 128 elements x box_rows x box_planes,
+// 128-byte swizzle.
 bool encode_planes(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
-                   uint64_t planes, uint32_t box_rows, uint32_t box_planes) {
+                   uint64_t planes, uint32_t box_rows, uint32_t box_planes,
+                   WeightType wt = kE4M3Map) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
+  const uint64_t row_bytes = cols * wt.bytes_num / wt.bytes_den;
   const cuuint64_t dims[3] = {cols, rows, planes};
-  const cuuint64_t strides[2] = {cols, rows * cols};
+  const cuuint64_t strides[2] = {row_bytes, rows * row_bytes};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageK), box_rows, box_planes};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(tm, wt.dt, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -121,16 +135,22 @@ int validate_config(const moe_config* c) {
   if (c->inter % 128 || c->inter < 256 || c->inter > 8192 || c->shared_inter != c->inter)
     return MOE_ERR_UNSUPPORTED;
   if (c->max_tokens > kMaxTokens) return MOE_ERR_UNSUPPORTED;
+  if (c->routed_format != MOE_ROUTED_E4M3 && c->routed_format != MOE_ROUTED_E2M1)
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
-int validate_weights(const moe_weights* w) {
+int validate_weights(const moe_weights* w, int routed_format) {
   const void* ptrs[] = {w->norm_w, w->gate_w, w->bias, w->w13, w->w13_s, w->w2,
                         w->w2_s,   w->sw13,   w->sw13_s, w->sw2, w->sw2_s};
   for (const void* p : ptrs) {
     if (!p) return MOE_ERR_ARG;
     if (!aligned16(p)) return MOE_ERR_ALIGN;
   }
+  // the 4-bit tensor copies want 32-byte aligned bases
+  if (routed_format == MOE_ROUTED_E2M1 && ((reinterpret_cast<uintptr_t>(w->w13) & 31) ||
+                                           (reinterpret_cast<uintptr_t>(w->w2) & 31)))
+    return MOE_ERR_ALIGN;
   return MOE_OK;
 }
 
@@ -204,7 +224,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   *out = nullptr;
   int rc = validate_config(cfg);
   if (rc) return rc;
-  rc = validate_weights(w);
+  rc = validate_weights(w, cfg->routed_format);
   if (rc) return rc;
 
   int ndev = 0;
@@ -258,6 +278,10 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   const size_t o_a13 = place(static_cast<size_t>(E + 1) * t13 * g13 * 16);
   const size_t o_a2 = place(static_cast<size_t>(E + 1) * t2 * g2 * 16);
   const size_t o_rd = place(static_cast<size_t>(E + 1) * 4);
+  const bool fp4 = cfg->routed_format == MOE_ROUTED_E2M1;
+  // MXFP4 routed experts: per-row scale images, 32 x 16 bytes per (tile, stage)
+  const size_t o_i13 = fp4 ? place(static_cast<size_t>(E) * t13 * g13 * 512) : 0;
+  const size_t o_i2 = fp4 ? place(static_cast<size_t>(E) * t2 * g2 * 512) : 0;
   h->scratch_bytes = off;
 
   cudaError_t err = cudaMalloc(&h->scratch, h->scratch_bytes);
@@ -285,6 +309,8 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->sfa13 = reinterpret_cast<uint4*>(b + o_a13);
   h->sfa2 = reinterpret_cast<uint4*>(b + o_a2);
   h->ready = reinterpret_cast<int*>(b + o_rd);
+  uint4* img13 = fp4 ? reinterpret_cast<uint4*>(b + o_i13) : nullptr;
+  uint4* img2 = fp4 ? reinterpret_cast<uint4*>(b + o_i2) : nullptr;
 
   err = cudaMemset(h->scratch, 0, h->scratch_bytes);
   if (err == cudaSuccess) err = router_setup();
@@ -297,6 +323,9 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
     sp.sw2_s = w->sw2_s;
     sp.sfa13 = h->sfa13;
     sp.sfa2 = h->sfa2;
+    sp.img13 = img13;
+    sp.img2 = img2;
+    sp.fp4 = fp4 ? 1 : 0;
     sp.E = E;
     sp.H = H;
     sp.I = I;
@@ -318,6 +347,9 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   pe.act = h->act;
   pe.sfa13 = h->sfa13;
   pe.sfa2 = h->sfa2;
+  pe.img13 = img13;
+  pe.img2 = img2;
+  pe.fp4 = fp4 ? 1 : 0;
   pe.xpan = h->xpan;
   pe.hpan = h->hpan;
   pe.part = h->part;
@@ -334,9 +366,10 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   pe.units_max = h->units_max;
   pe.rows_max = h->rows_max;
   // w13 as [2E halves][I rows][H]: one box = 64 gate rows over the 64 matching up rows
-  bool ok = encode_planes(&pe.tm_w13, w->w13, H, I, 2ull * E, 64, 2) &&
+  const WeightType wt = fp4 ? kE2M1Map : kE4M3Map;
+  bool ok = encode_planes(&pe.tm_w13, w->w13, H, I, 2ull * E, 64, 2, wt) &&
             encode_planes(&pe.tm_w13_shared, w->sw13, H, I, 2, 64, 2) &&
-            encode_rows(&pe.tm_w2, w->w2, I, static_cast<uint64_t>(E) * H, kTileM) &&
+            encode_rows(&pe.tm_w2, w->w2, I, static_cast<uint64_t>(E) * H, kTileM, wt) &&
             encode_rows(&pe.tm_w2_shared, w->sw2, I, static_cast<uint64_t>(H), kTileM);
   if (!ok) {
     cudaFree(h->scratch);

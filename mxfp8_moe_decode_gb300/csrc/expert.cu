@@ -29,9 +29,9 @@
 //
 // Per CTA (one per SM, 288 threads):
 //  warp 8 lane 0, the scheduler, claims the CTA's tasks one ahead of the
-//    producer (the next one when the producer has 4 stages of the current one
-//    left to issue, so that a w2 task is rarely claimed long before its unit
-//    can be done), posts each id with its unit's table entry to a small queue
+//    producer (the next one when the producer has kClaimLead stages of the
+//    current one left to issue, so that a w2 task is rarely claimed long
+//    before its unit can be done), posts each id with its unit's table entry to a small queue
 //    in shared memory, and for a w2 task waits (device scope) for the unit's
 //    readiness and publishes it in shared memory. A device-scope wait in the
 //    producer thread would also wait for its copies in flight.
@@ -53,6 +53,17 @@
 //    same per-thread rate.
 //  warps 4-7 drain the double-buffered accumulators (each reads its 32-lane
 //    quarter).
+//
+// MXFP4 routed experts ("vllm.models.deepseek_v41.amd.mono.runner",
+// MonoLayerWeights: w13 / w2 float4_e2m1fn_x2 with one E8M0 per row per 32
+// columns): the weight box is a 4-bit tensor copy that spreads each 16 codes
+// into a 16-byte shared-memory unit (8 bytes of codes, 8 of gap), the form
+// kind::mxf8f6f4 reads for an E2M1 operand, so a stage has the same layout
+// and descriptors as with E4M3 and only the instruction descriptor's A
+// format changes. The per-row codes differ across all 128 rows of a tile, so
+// each stage's scale image (lane i, cell c = row 32 c + i) is prepacked at
+// creation and copied by the producer with the weights (the image warp only
+// marks those slots ready). The shared expert stays E4M3.
 // Every mbarrier and readiness wait is bounded; on a timeout the CTA records
 // kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
 //
@@ -360,8 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         if (task < 0) break;  // -1: no more tasks; -2: a wait gave up
         const int nt = (a.z + 15) & ~15;
         const uint32_t pbytes = kPanelRows + nt * 128;  // the panel's used part
-        const uint32_t bytes = kABytes + pbytes;
         const bool shared_e = a.x == p.E;
+        // MXFP4 routed weights: the stage's per-row scale image comes with
+        // the weights (one 512-byte copy) instead of from the image warp; a
+        // 4-bit weight box counts its global bytes (two codes per byte), half
+        // of what it fills in shared memory
+        const bool img = p.fp4 && !shared_e;
+        const uint32_t bytes = (img ? kABytes / 2 + kImgBytes : kABytes) + pbytes;
+        const uint4* img_src =
+            !img ? nullptr
+                 : (k.phase ? p.img2 + ((static_cast<size_t>(a.x) * p.t2 + k.t) * p.g2 + k.g0) * 32
+                            : p.img13 + ((static_cast<size_t>(a.x) * p.t13 + k.t) * p.g13 + k.g0) * 32);
         const int G = k.gn;
         const int panels = k.phase ? p.g2 : p.g13;  // per unit (h) or expert (x)
         // x panels are kept per expert id (a lone token's experts all read
@@ -399,6 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
             ptx::tma_load_2d(sa, shared_e ? &p.tm_w2_shared : &p.tm_w2, x,
                              (shared_e ? 0 : a.x * p.hidden) + kTileM * k.t, full, pol_w);
           }
+          if (img)
+            ptx::bulk_load(ptx::smem_u32(smem + kOffSfa + s * kImgBytes), img_src + g * 32,
+                           kImgBytes, full, pol_w);
           if (b_ok) {
             issue_b(g, s);
           } else {
@@ -450,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         const int task = take_task(bars, misc, j, abort, &a, &k);
         if (task < 0) break;
         const int nt = (a.z + 15) & ~15;
+        const uint32_t a_fmt = (p.fp4 && a.x != p.E) ? ptx::kFmtE2M1 : ptx::kFmtE4M3;
         const int G = k.gn;  // at least 2: both issuers write their accumulator
         const int acc = lt & 1;
         const uint32_t use = static_cast<uint32_t>(lt) >> 1;
@@ -480,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             ptx::tc_mma_mxf8(d_tmem, ptx::sdesc_k128_sw128(sa + 32 * kk),
-                             ptx::sdesc_k128_sw128(sb + 32 * kk), ptx::idesc_mxf8_e4m3(nt, kk), sf_a,
+                             ptx::sdesc_k128_sw128(sb + 32 * kk), ptx::idesc_mxf8(nt, kk, a_fmt), sf_a,
                              sf_b, (g > h) || kk != 0);
           }
           ptx::tc_commit(ptx::smem_u32(&bars->empty[s]));
@@ -514,18 +538,24 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       k.gn = __shfl_sync(0xffffffffu, k0.gn, 0);
       k.half = __shfl_sync(0xffffffffu, k0.half, 0);
       const int G = k.gn;
+      // MXFP4 routed weights: the producer copies the stage's image itself
+      const bool copied = p.fp4 && ex != p.E;
       const uint4* sfa = (k.phase ? p.sfa2 + (static_cast<size_t>(ex) * p.t2 + k.t) * p.g2
                                   : p.sfa13 + (static_cast<size_t>(ex) * p.t13 + k.t) * p.g13) +
                          k.g0;
       const uint4 zero = make_uint4(0, 0, 0, 0);
-      const uint4 e0 = lane < G ? __ldg(sfa + lane) : zero;  // stages lane and lane + 32
-      const uint4 e1 = lane + 32 < G ? __ldg(sfa + lane + 32) : zero;
+      const uint4 e0 = !copied && lane < G ? __ldg(sfa + lane) : zero;  // stages lane, lane + 32
+      const uint4 e1 = !copied && lane + 32 < G ? __ldg(sfa + lane + 32) : zero;
       for (int g = 0; g < G; ++g, ++it) {
         const int s = it % kStages;
         const uint32_t round = it / kStages;
         if (!warp_wait(ptx::smem_u32(&bars->empty[s]), (round & 1) ^ 1, abort)) {
           ok = false;
           break;
+        }
+        if (copied) {
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->sfa_rdy[s]));
+          continue;
         }
         const uint4 src = g < 32 ? e0 : e1;
         uint4 v;

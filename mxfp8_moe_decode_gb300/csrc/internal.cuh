@@ -157,6 +157,9 @@ struct ExpertParams {
   ActiveExpert* act;          // [units] the unit table, written by CTA 0 (diagnostics)
   const uint4* sfa13;         // [E + 1][I/64][H/128] compact weight-scale entries
   const uint4* sfa2;          // [E + 1][H/128][I/128]
+  const uint4* img13;         // MXFP4 routed experts: [E][I/64][H/128][32] per-row scale
+  const uint4* img2;          // images ([E][H/128][I/128][32]), else null
+  int fp4;                    // routed experts are E2M1 with per-row scales
   const uint8_t* xpan;        // [E + 1][H/128] x panels by expert id (the routed ones written by
                               // the top-k kernel, the shared one -- rows = tokens -- by the seam;
                               // at M = 1 every unit reads the shared one: its single row is token 0)
@@ -209,6 +212,10 @@ struct SfaPackParams {
   const uint8_t* sw2_s;
   uint4* sfa13;
   uint4* sfa2;
+  uint4* img13;  // MXFP4 routed experts: per-row scale images (else null)
+  uint4* img2;
+  int fp4;       // routed w13_s / w2_s hold per-row codes: only the shared
+                 // expert gets compact 32 x 32 entries
   int E, H, I;
 };
 

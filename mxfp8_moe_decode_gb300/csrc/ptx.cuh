@@ -257,17 +257,21 @@ __device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B (both K-major),
-// UE8M0 scale factors, M = 128, the given N; sf_id selects the byte of the
-// 32-bit scale cells used for both operands.
-__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(uint32_t n, uint32_t sf_id) {
-  return (sf_id << 4)              // B scale-factor byte
-         | (0u << 7) | (0u << 10)  // A, B format: E4M3
-         | (0u << 15) | (0u << 16) // A, B K-major
-         | ((n >> 3) << 17)        // N / 8
-         | (1u << 23)              // scale-factor type UE8M0
-         | ((128u >> 4) << 24)     // M / 16
-         | (sf_id << 29);          // A scale-factor byte
+// Operand formats of kind::mxf8f6f4 in the instruction descriptor.
+constexpr uint32_t kFmtE4M3 = 0;
+constexpr uint32_t kFmtE2M1 = 5;
+
+// Instruction descriptor of kind::mxf8f6f4 with A in format a_fmt (E4M3 or
+// E2M1) and E4M3 B (both K-major), UE8M0 scale factors, M = 128, the given N;
+// sf_id selects the byte of the 32-bit scale cells used for both operands.
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t n, uint32_t sf_id, uint32_t a_fmt) {
+  return (sf_id << 4)                  // B scale-factor byte
+         | (a_fmt << 7) | (kFmtE4M3 << 10)  // A, B formats
+         | (0u << 15) | (0u << 16)     // A, B K-major
+         | ((n >> 3) << 17)            // N / 8
+         | (1u << 23)                  // scale-factor type UE8M0
+         | ((128u >> 4) << 24)         // M / 16
+         | (sf_id << 29);              // A scale-factor byte
 }
 
 }  // namespace ptx

@@ -22,6 +22,8 @@ consumer):
   inside E4M3's range), code = 127 + e - 8, bytes = torch's float8_e4m3fn
   cast of w / scale. This is a synthesis rule for the weights, which the
   pages receive already quantised; it is not the activation code of the step.
+  MXFP4 routed experts (``routed="e2m1"``): per row and 32 columns a scale
+  2^(e - 2), values rounded to the nearest E2M1 value (``_row_quant_fp4``).
 
 bf16 rounding of the host draws uses torch's bfloat16 cast (round to nearest
 even).
@@ -48,10 +50,13 @@ class MoeDims:
     shared_inter: int
     max_tokens: int = 48
     eps: float = 1e-6
+    routed: str = "e4m3"  # routed weights: "e4m3" (32 x 32 scales) or "e2m1" (1 x 32 per row)
 
     def expert_bytes(self) -> int:
         """Weight + scale bytes of one routed expert (w13 and w2)."""
         h, i = self.hidden, self.inter
+        if self.routed == "e2m1":
+            return (2 * i * h + h * i) // 2 + (2 * i * h + h * i) // 32
         return 2 * i * h + (2 * i // 32) * (h // 32) + h * i + (h // 32) * (i // 32)
 
     def shared_bytes(self) -> int:
@@ -78,6 +83,10 @@ FULL = MoeDims(hidden=5120, experts=256, topk=8, inter=2048, shared_inter=2048)
 # (gate_w [384, 5120]); its top-k and unsharded intermediate are not printed:
 # these take k = 8 and I = 2048 as above, with E4M3 routed weights.
 E384 = MoeDims(hidden=5120, experts=384, topk=8, inter=2048, shared_inter=2048)
+# ... and its routed experts in the page's format: E2M1 pairs with one E8M0
+# code per row per 32 columns (the shared expert stays E4M3, 32 x 32 blocks)
+E384_FP4 = MoeDims(hidden=5120, experts=384, topk=8, inter=2048, shared_inter=2048,
+                   routed="e2m1")
 
 WORKLOADS = {
     w.name: w
@@ -98,6 +107,14 @@ WORKLOADS = {
                  "384-expert layer, single-token decode, M=1, H5120 E384 k8 I2048"),
         Workload("full_e384_m48", E384, 48, 6, "uniform",
                  "384-expert layer, M=48, uniform bias"),
+        Workload("tiny_fp4", MoeDims(1024, 64, 4, 512, 512, routed="e2m1"), 1, 7, "normal",
+                 "tiny layer with MXFP4 routed experts, H1024 E64 k4 I512"),
+        Workload("small_fp4_m16", MoeDims(5120, 64, 4, 1024, 1024, routed="e2m1"), 16, 8,
+                 "normal", "small-expert layer with MXFP4 routed experts, M=16"),
+        Workload("full_e384_fp4_m1", E384_FP4, 1, 5, "uniform",
+                 "384-expert layer, MXFP4 routed experts, M=1"),
+        Workload("full_e384_fp4_m48", E384_FP4, 48, 6, "uniform",
+                 "384-expert layer, MXFP4 routed experts, M=48, uniform bias"),
     ]
 }
 
@@ -171,6 +188,34 @@ def _block_quant(w: torch.Tensor):
     return b, code.to(torch.uint8)
 
 
+# E2M1 magnitudes in code order (codes 0..7) and the midpoints between them
+_E2M1_MAG = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+_E2M1_MID = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+def _row_quant_fp4(w: torch.Tensor):
+    """fp32 [R, C] -> (E2M1 pairs uint8 [R, C/2], codes uint8 [R, C/32]): per
+    row and 32 columns a power-of-two scale 2^(e - 2) with 2^(e-1) <= amax <
+    2^e (scaled magnitudes below 4), code 127 + e - 2, values rounded to the
+    nearest E2M1 value (ties to the even code); element 2j in the low nibble
+    of byte j. A synthesis rule for the inputs, like _block_quant."""
+    r, c = w.shape
+    blocks = w.view(r, c // 32, 32)
+    amax = blocks.abs().amax(dim=2)
+    _, e = torch.frexp(amax)
+    code = (127 + e.to(torch.int32) - 2).clamp(1, 254)
+    mul = ((254 - code) << 23).to(torch.int32).view(torch.float32)
+    v = (blocks * mul[..., None]).view(r, c)
+    a = v.abs()
+    mid = torch.tensor(_E2M1_MID, dtype=a.dtype, device=a.device)
+    k = torch.bucketize(a, mid)  # a <= mid[k] and a > mid[k - 1]
+    tie = (k < len(_E2M1_MID)) & (a == mid[k.clamp(max=len(_E2M1_MID) - 1)]) & (k % 2 == 1)
+    k = torch.where(tie, k + 1, k)
+    nib = (k | (torch.signbit(v).to(k.dtype) << 3)).to(torch.uint8)
+    packed = nib[:, 0::2] | (nib[:, 1::2] << 4)
+    return packed.contiguous(), code.to(torch.uint8)
+
+
 def _expert_gen(device, seed: int, tag: int, e: int) -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed((seed * 1_000_003 + tag * 65_537 + e) & 0x7FFF_FFFF_FFFF_FFFF)
@@ -181,25 +226,33 @@ def expert_weights(wl: Workload, device="cpu", experts=None, sigma: float = 0.02
     """Routed + shared expert weights on ``device``.
 
     Returns w13 uint8 [E, 2I, H], w13_s uint8 [E, 2I/32, H/32], w2 uint8
-    [E, H, I], w2_s uint8 [E, H/32, I/32] and the shared expert's sw13 / sw13_s
-    / sw2 / sw2_s without the E axis. ``experts``: optional iterable of routed
+    [E, H, I], w2_s uint8 [E, H/32, I/32] (E2M1 routed experts: w13 [E, 2I,
+    H/2], w13_s [E, 2I, H/32], w2 [E, H, I/2], w2_s [E, H, I/32]) and the
+    shared expert's sw13 / sw13_s / sw2 / sw2_s (E4M3) without the E axis. ``experts``: optional iterable of routed
     expert ids to draw (others stay zero) -- each expert has its own stream, so
     a subset draws the same values as the whole.
     """
     d = wl.dims
     h, i, ish = d.hidden, d.inter, d.shared_inter
     dev = torch.device(device)
-    w13 = torch.zeros(d.experts, 2 * i, h, dtype=torch.uint8, device=dev)
-    w13_s = torch.zeros(d.experts, 2 * i // 32, h // 32, dtype=torch.uint8, device=dev)
-    w2 = torch.zeros(d.experts, h, i, dtype=torch.uint8, device=dev)
-    w2_s = torch.zeros(d.experts, h // 32, i // 32, dtype=torch.uint8, device=dev)
+    fp4 = d.routed == "e2m1"
+    if fp4:  # E2M1 pairs, one code per row per 32 columns
+        w13 = torch.zeros(d.experts, 2 * i, h // 2, dtype=torch.uint8, device=dev)
+        w13_s = torch.zeros(d.experts, 2 * i, h // 32, dtype=torch.uint8, device=dev)
+        w2 = torch.zeros(d.experts, h, i // 2, dtype=torch.uint8, device=dev)
+        w2_s = torch.zeros(d.experts, h, i // 32, dtype=torch.uint8, device=dev)
+    else:
+        w13 = torch.zeros(d.experts, 2 * i, h, dtype=torch.uint8, device=dev)
+        w13_s = torch.zeros(d.experts, 2 * i // 32, h // 32, dtype=torch.uint8, device=dev)
+        w2 = torch.zeros(d.experts, h, i, dtype=torch.uint8, device=dev)
+        w2_s = torch.zeros(d.experts, h // 32, i // 32, dtype=torch.uint8, device=dev)
+    quant = _row_quant_fp4 if fp4 else _block_quant
     todo = range(d.experts) if experts is None else sorted(set(int(e) for e in experts))
     for e in todo:
         g = _expert_gen(dev, wl.seed, _T_W13, e)
-        w13[e], w13_s[e] = _block_quant(
-            torch.randn(2 * i, h, generator=g, device=dev) * sigma)
+        w13[e], w13_s[e] = quant(torch.randn(2 * i, h, generator=g, device=dev) * sigma)
         g = _expert_gen(dev, wl.seed, _T_W2, e)
-        w2[e], w2_s[e] = _block_quant(torch.randn(h, i, generator=g, device=dev) * sigma)
+        w2[e], w2_s[e] = quant(torch.randn(h, i, generator=g, device=dev) * sigma)
     g = _expert_gen(dev, wl.seed, _T_SW13, 0)
     sw13, sw13_s = _block_quant(torch.randn(2 * ish, h, generator=g, device=dev) * sigma)
     g = _expert_gen(dev, wl.seed, _T_SW2, 0)

@@ -54,13 +54,16 @@ class Layer:
         weights = {"norm_w": self.ri["norm_w"].to(self.dev), "gate_w": self.ri["gate_w"].to(self.dev),
                    "bias": self.ri["bias"].to(self.dev), **self.ew}
         self.layer = MoeDecode(d.hidden, d.experts, d.topk, d.inter, weights,
-                               max_tokens=max_tokens or d.max_tokens, eps=d.eps)
+                               max_tokens=max_tokens or d.max_tokens, eps=d.eps,
+                               routed=d.routed)
         self._cache: dict = {}
 
     def expert(self, e: int) -> O.ExpertWeights:
         if e not in self._cache:
             ew = self.ew
-            self._cache[e] = O.ExpertWeights.from_quantised(
+            make = (O.ExpertWeights.from_fp4 if self.wl.dims.routed == "e2m1"
+                    else O.ExpertWeights.from_quantised)
+            self._cache[e] = make(
                 ew["w13"][e].cpu().numpy(), ew["w13_s"][e].cpu().numpy(),
                 ew["w2"][e].cpu().numpy(), ew["w2_s"][e].cpu().numpy())
         return self._cache[e]

@@ -104,3 +104,16 @@ def test_attn_seam_argument_checks_without_a_gpu(L):
         assert f(x, w, 4, h, 1e-6, b, c, y, None) == MOE_ERR_UNSUPPORTED, h
     assert f(x, w, 4, 256, -1.0, b, c, y, None) == MOE_ERR_ARG
     assert f(x, w, 4, 256, float("nan"), b, c, y, None) == MOE_ERR_ARG
+
+
+def test_create_checks_the_routed_format_without_a_gpu(L):
+    h = ctypes.c_void_p()
+    w = _weights()
+    rc = L.moe_create(ctypes.byref(_cfg(routed_format=2)), ctypes.byref(w), 0, ctypes.byref(h))
+    assert rc == MOE_ERR_UNSUPPORTED and h.value is None
+    # MXFP4 routed weights must start on 32 bytes (the 4-bit tensor copies)
+    for key in ("w13", "w2"):
+        wa = _weights()
+        setattr(wa, key, 0x10010)
+        rc = L.moe_create(ctypes.byref(_cfg(routed_format=1)), ctypes.byref(wa), 0, ctypes.byref(h))
+        assert rc == MOE_ERR_ALIGN and h.value is None, key

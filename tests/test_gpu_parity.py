@@ -161,6 +161,19 @@ def test_unit_table(name, m):
         L.close()
 
 
+@pytest.mark.parametrize("m", [1, 2, 5, 16, 17, 33, 48])
+def test_fp4_routed_experts(m):
+    """MXFP4 routed experts (E2M1 weights, per-row 1 x 32 codes) against the
+    oracle's per-row dequantisation, every MMA N bucket and ragged rows."""
+    L = Layer(W.WORKLOADS["tiny_fp4"])
+    try:
+        x, _ = gapped_tokens(L.wl, L.ri, m=m)
+        err, _ = check(L, x, label=f"tiny_fp4 m={m}")
+        print(f"tiny_fp4 m={m}: rel err {err:.2e}")
+    finally:
+        L.close()
+
+
 def test_step_launches(tiny):
     """Steps of at most 4 tokens run the seam inside the router: one launch fewer."""
     L = tiny.layer
@@ -182,7 +195,9 @@ def test_small_m4():
                                          ("full_m48_uniform", [0, 23, 47]),
                                          ("full_m48_zipf", [0, 23, 47]),
                                          ("full_e384_m1", None),
-                                         ("full_e384_m48", [0, 23, 47])])
+                                         ("full_e384_m48", [0, 23, 47]),
+                                         ("full_e384_fp4_m1", None),
+                                         ("full_e384_fp4_m48", [0, 23, 47])])
 def test_full_size(name, sample):
     L = Layer(W.WORKLOADS[name])
     try:
