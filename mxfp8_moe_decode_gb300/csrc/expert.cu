@@ -307,6 +307,9 @@ __device__ __forceinline__ bool wait_seq(const int* seq, int j, volatile int* ab
   }
 }
 
+// kFp4: the routed experts are MXFP4 (E2M1 with per-row scale images); the
+// E4M3 instantiation carries none of that path's code.
+template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_constant__ ExpertParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         // the weights (one 512-byte copy) instead of from the image warp; a
         // 4-bit weight box counts its global bytes (two codes per byte), half
         // of what it fills in shared memory
-        const bool img = p.fp4 && !shared_e;
+        const bool img = kFp4 && !shared_e;
         const uint32_t bytes = (img ? kABytes / 2 + kImgBytes : kABytes) + pbytes;
         const uint4* img_src =
             !img ? nullptr
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         const int task = take_task(bars, misc, j, abort, &a, &k);
         if (task < 0) break;
         const int nt = (a.z + 15) & ~15;
-        const uint32_t a_fmt = (p.fp4 && a.x != p.E) ? ptx::kFmtE2M1 : ptx::kFmtE4M3;
+        const uint32_t a_fmt = (kFp4 && a.x != p.E) ? ptx::kFmtE2M1 : ptx::kFmtE4M3;
         const int G = k.gn;  // at least 2: both issuers write their accumulator
         const int acc = lt & 1;
         const uint32_t use = static_cast<uint32_t>(lt) >> 1;
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       k.half = __shfl_sync(0xffffffffu, k0.half, 0);
       const int G = k.gn;
       // MXFP4 routed weights: the producer copies the stage's image itself
-      const bool copied = p.fp4 && ex != p.E;
+      const bool copied = kFp4 && ex != p.E;
       const uint4* sfa = (k.phase ? p.sfa2 + (static_cast<size_t>(ex) * p.t2 + k.t) * p.g2
                                   : p.sfa13 + (static_cast<size_t>(ex) * p.t13 + k.t) * p.g13) +
                          k.g0;
@@ -811,12 +814,18 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
 size_t expert_smem_bytes(int) { return kSmemBytes; }
 
 cudaError_t expert_kernel_setup() {
-  return cudaFuncSetAttribute(expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemBytes));
+  cudaError_t e = cudaFuncSetAttribute(expert_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+  return e;
 }
 
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s) {
-  return launch_pdl(expert_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+  return p.fp4 ? launch_pdl(expert_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, p)
+               : launch_pdl(expert_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
 }
 
 }  // namespace moe
