@@ -246,6 +246,33 @@ def test_max_hidden_and_inter():
         L.close()
 
 
+def test_fp4_limits():
+    # MXFP4 routed experts at the largest widths (64 K stages per task, 4-bit
+    # rows of 4 KB) and with 512 experts at top-16 and the smallest widths
+    # (4-bit rows of 128 bytes: the copy's minimum box row)
+    wl = W.Workload("limits_fp4_h8192", W.MoeDims(8192, 32, 2, 8192, 8192, routed="e2m1"), 2, 6,
+                    "normal")
+    L = Layer(wl)
+    try:
+        x, _ = gapped_tokens(L.wl, L.ri)
+        err, _ = check(L, x, tokens=[0], label="fp4 H8192 I8192")
+        print(f"fp4 H8192 I8192: rel err {err:.2e}")
+    finally:
+        L.close()
+    wl = W.Workload("limits_fp4_e512", W.MoeDims(256, 512, 16, 256, 256, routed="e2m1"), 48, 5,
+                    "normal")
+    perm = np.random.default_rng([5, 99]).permutation(512)
+    bias = torch.zeros(512, dtype=torch.float32)
+    bias[torch.from_numpy(perm)] = -0.05 * torch.arange(512, dtype=torch.float32)
+    L = Layer(wl, bias=bias)
+    try:
+        x, _ = gapped_tokens(L.wl, L.ri)
+        err, _ = check(L, x, label="fp4 E512 k16")
+        print(f"fp4 E512 k16 M48: rel err {err:.2e}")
+    finally:
+        L.close()
+
+
 def test_every_token_on_the_same_experts():
     # a bias that sends all 48 tokens to the same k experts: every routed unit
     # has 48 rows (MMA N = 48), the other experts are idle
