@@ -74,9 +74,9 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
+def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+    was taken on the current kernel source and on this workload (else None)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
@@ -84,6 +84,8 @@ def ncu_traffic(kernel: str):
         d = json.load(f)
     e = d.get(kernel)
     if not e or e.get("source_hash") != kernel_hash():
+        return None
+    if str(e.get("workload", "")).split(" ")[0] != workload:
         return None
     return e.get("bytes_per_launch")
 
@@ -351,7 +353,7 @@ def run_gpu(args):
     ach = exp_bytes / (kmean[ix] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": "experts", "achieved": round(ach, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "traffic": ncu_traffic("experts"),
+                "traffic": ncu_traffic("experts", wl.name),
                 "alg_bytes_per_launch": exp_bytes,
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
                 if peaks["source"] == "measured" else "fallback 6.8 TB/s"}
