@@ -43,7 +43,7 @@ class Layer:
     weight tensors (copied to the host one expert at a time)."""
 
     def __init__(self, wl: W.Workload, device="cuda:0", max_tokens: int | None = None,
-                 bias: torch.Tensor | None = None):
+                 bias: torch.Tensor | None = None, edit_weights=None):
         self.wl = wl
         d = wl.dims
         self.dev = torch.device(device)
@@ -51,6 +51,8 @@ class Layer:
         if bias is not None:  # a routing scenario the workload's bias does not give
             self.ri["bias"] = bias.to(torch.float32).cpu()
         self.ew = W.expert_weights(wl, device=self.dev)
+        if edit_weights is not None:  # a weight pattern the synthesis rule does not give
+            edit_weights(self.ew)
         weights = {"norm_w": self.ri["norm_w"].to(self.dev), "gate_w": self.ri["gate_w"].to(self.dev),
                    "bias": self.ri["bias"].to(self.dev), **self.ew}
         self.layer = MoeDecode(d.hidden, d.experts, d.topk, d.inter, weights,

@@ -174,6 +174,30 @@ def test_fp4_routed_experts(m):
         L.close()
 
 
+def test_fp4_every_code():
+    """The synthesis rule never draws E2M1 code 7 (6.0): routed weights of
+    uniformly random bytes (all 16 codes in both nibbles) with per-row codes
+    spread over 2^-10 .. 2^-6, against the oracle's decoding."""
+    def edit(ew):
+        g = torch.Generator(device=ew["w13"].device).manual_seed(1234)
+        for k in ("w13", "w2"):
+            ew[k].copy_(torch.randint(0, 256, ew[k].shape, generator=g, device=ew[k].device,
+                                      dtype=torch.int32).to(torch.uint8))
+            ew[k + "_s"].copy_(torch.randint(117, 122, ew[k + "_s"].shape, generator=g,
+                                             device=ew[k].device, dtype=torch.int32)
+                               .to(torch.uint8))
+    L = Layer(W.WORKLOADS["tiny_fp4"], edit_weights=edit)
+    try:
+        w = L.ew["w13"].cpu().numpy()
+        assert len(np.unique(w & 15)) == 16 and len(np.unique(w >> 4)) == 16
+        for m in (1, 17, 48):
+            x, _ = gapped_tokens(L.wl, L.ri, m=m)
+            err, _ = check(L, x, label=f"fp4 every code m={m}")
+            print(f"fp4 every code m={m}: rel err {err:.2e}")
+    finally:
+        L.close()
+
+
 def test_step_launches(tiny):
     """Steps of at most 4 tokens run the seam inside the router: one launch fewer."""
     L = tiny.layer
