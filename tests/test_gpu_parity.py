@@ -198,6 +198,32 @@ def test_fp4_every_code():
         L.close()
 
 
+def test_e4m3_every_code():
+    """The synthesis rule keeps scaled weights below 256: routed and shared
+    weights of uniformly random E4M3 bytes (every finite code, NaN bytes
+    0x7F / 0xFF excluded) with block codes 113..117, against the oracle."""
+    def edit(ew):
+        g = torch.Generator(device=ew["w13"].device).manual_seed(4321)
+        for k in ("w13", "w2", "sw13", "sw2"):
+            b = torch.randint(0, 254, ew[k].shape, generator=g, device=ew[k].device,
+                              dtype=torch.int32)
+            b = torch.where(b >= 0x7F, b + 1, b)  # skip 0x7F; 0xFF is never drawn
+            ew[k].copy_(b.to(torch.uint8))
+            ew[k + "_s"].copy_(torch.randint(113, 118, ew[k + "_s"].shape, generator=g,
+                                             device=ew[k].device, dtype=torch.int32)
+                               .to(torch.uint8))
+    L = Layer(W.WORKLOADS["tiny_m1"], edit_weights=edit)
+    try:
+        w = L.ew["w13"].cpu().numpy()
+        assert len(np.unique(w)) == 254 and not np.any((w == 0x7F) | (w == 0xFF))
+        for m in (1, 17, 48):
+            x, _ = gapped_tokens(L.wl, L.ri, m=m)
+            err, _ = check(L, x, label=f"e4m3 every code m={m}")
+            print(f"e4m3 every code m={m}: rel err {err:.2e}")
+    finally:
+        L.close()
+
+
 def test_step_launches(tiny):
     """Steps of at most 4 tokens run the seam inside the router: one launch fewer."""
     L = tiny.layer
