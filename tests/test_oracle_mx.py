@@ -157,3 +157,31 @@ def test_dequant_fp4_rows_per_row_scales():
             assert got[r, c] == want, (r, c, got[r, c], want)
     with pytest.raises(ValueError):
         dequant_fp4_rows(packed, code[:, :1])
+
+
+def test_fp4_synthesis_rule():
+    """The input generator's MXFP4 weights (workloads._row_quant_fp4), decoded
+    by the oracle: each value within half an E2M1 spacing of its draw (a
+    quarter-spacing of the scale below 2, a half above), ties to the even code,
+    codes 127 + e - 2 for 2^(e-1) <= amax < 2^e."""
+    import torch
+    from mxfp8_moe_decode_gb300 import workloads as W
+    from oracle.mx import dequant_fp4_rows
+    g = torch.Generator().manual_seed(3)
+    w = torch.randn(16, 256, generator=g) * 0.02
+    w[0, :32] = 0.0
+    w[1, :8] = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, -1.25, 3.9]) * 2.0 ** -6
+    p, c = W._row_quant_fp4(w)
+    assert p.shape == (16, 128) and c.shape == (16, 8)
+    got = dequant_fp4_rows(p.numpy(), c.numpy())
+    v = w.double().numpy()
+    scale = np.repeat(2.0 ** (c.numpy().astype(np.int64) - 127), 32, axis=1)
+    q = v / scale
+    spacing = np.where(np.abs(q) < 2, 0.5, 1.0)
+    assert np.all(np.abs(got / scale - q) <= spacing / 2 + 1e-12)
+    amax = np.abs(v.reshape(16, 8, 32)).max(axis=2)
+    nz = amax > 0
+    e = np.floor(np.log2(amax[nz])) + 1
+    assert np.array_equal(c.numpy()[nz].astype(np.int64), (127 + e - 2).astype(np.int64))
+    # the hand-set ties (amax 3.9 * 2^-6 -> scale 2^-6): to the even code
+    assert got[1, :8].tolist() == [x * 2.0 ** -6 for x in (0.0, 1.0, 1.0, 2.0, 2.0, 4.0, -1.0, 4.0)]
