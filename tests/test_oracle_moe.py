@@ -225,6 +225,27 @@ def test_one_token_one_expert_reduction():
     assert np.array_equal(res.out, moe.bf16_rne(y))
 
 
+def test_identical_routed_experts_sum_once():
+    # every routed expert the same: whatever the router picks, the k picks'
+    # normalised weights sum to 1, so out = bf16(y_routed + y_shared); a
+    # dropped pick, an unnormalised weight or a shared term added twice fails
+    rng = np.random.default_rng(12)
+    experts, shared, norm_w, gate_w, bias = _tiny_layer(rng)
+    same = experts[0]
+    x = moe.bf16_rne(rng.standard_normal((3, 64)))
+    for k in (1, 2, 3):
+        res = moe.decode_step(x, norm_w, gate_w, bias, k, lambda e: same, lambda: shared)
+        assert np.allclose(res.routing.weights.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+        xh = dequant_rows(res.x8, res.codes)
+        y = moe.expert(xh, same)[0]
+        ysh = moe.expert(xh, shared)[0]
+        # the weights sum to 1 only up to rounding: compare before the bf16 step
+        acc = np.einsum("mk,mh->mh", res.routing.weights, y) + ysh
+        want = moe.bf16_rne(acc)
+        assert np.array_equal(res.out, want), k
+        assert np.allclose(acc, y + ysh, rtol=1e-14, atol=1e-14)
+
+
 def test_step_token_permutation_invariance():
     rng = np.random.default_rng(9)
     experts, shared, norm_w, gate_w, bias = _tiny_layer(rng)
