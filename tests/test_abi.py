@@ -117,3 +117,15 @@ def test_create_checks_the_routed_format_without_a_gpu(L):
         setattr(wa, key, 0x10010)
         rc = L.moe_create(ctypes.byref(_cfg(routed_format=1)), ctypes.byref(wa), 0, ctypes.byref(h))
         assert rc == MOE_ERR_ALIGN and h.value is None, key
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """The binding only loads the in-tree library: without it every entry
+    raises instead of falling back to anything else."""
+    import mxfp8_moe_decode_gb300.api as api
+    monkeypatch.setattr(_lib, "_LIB", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "absent" / "libmoe_decode.so"))
+    with pytest.raises(FileNotFoundError):
+        _lib.lib()
+    with pytest.raises(FileNotFoundError):
+        api.kernel_names()
