@@ -148,9 +148,13 @@ typedef struct moe_handle moe_handle;
  * step's scratch for cfg->max_tokens rows (all of it, up front), packs the
  * weight scales, encodes the TMA descriptors, and synchronises the device.
  * On success *out holds a new handle. Errors: MOE_ERR_ARG (null / bad dims),
- * MOE_ERR_UNSUPPORTED (dims outside the limits above), MOE_ERR_ALIGN,
- * MOE_ERR_DEVICE, MOE_ERR_CUDA, MOE_ERR_CAPTURE (the legacy stream of
- * `device` is being captured: creation allocates and synchronises).
+ * MOE_ERR_UNSUPPORTED (dims or routed_format outside the limits above),
+ * MOE_ERR_ALIGN (a weight pointer not 16-byte aligned, or with
+ * MOE_ROUTED_E2M1 the routed w13 / w2 not 32-byte aligned), MOE_ERR_DEVICE,
+ * MOE_ERR_CUDA, MOE_ERR_CAPTURE (the legacy stream of `device` is being
+ * captured: creation allocates and synchronises). With MOE_ROUTED_E2M1 the
+ * handle also holds the routed experts' per-row scale codes regrouped for the
+ * tensor cores (as many bytes as w13_s and w2_s).
  */
 int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_handle** out);
 
