@@ -38,11 +38,12 @@ those fp32 values in 32-groups with the same code and E4M3 rule.
 Pins (tests/test_oracle_moe.py): hand-worked RMSNorm values
 (tests/golden/rmsnorm_cases.txt), silu closed forms, brute-force top-k over
 all k-subsets on small E, an expert built from hand-chosen bytes and codes
-whose result is worked out by hand, the one-token / one-expert reduction,
-identical routed experts (the picks' weights sum to one: out = bf16(y + y_shared)
-whatever is picked), and token-permutation invariance of the whole step. The composed step has no
-worked example on the pages: its end-to-end numbers are "parity unpinned"
-beyond what those pins fix.
+whose result is worked out by hand, and, for the composed step, three
+invariants: the one-token / one-expert reduction, identical routed experts
+(the picks' weights sum to one: out = bf16(y + y_shared) whatever is
+picked) and token-permutation invariance. The composed step has no worked
+example on the pages: beyond what those pins and invariants fix, its
+end-to-end numbers are "parity unpinned".
 """
 
 from __future__ import annotations
