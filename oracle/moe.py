@@ -37,13 +37,18 @@ those fp32 values in 32-groups with the same code and E4M3 rule.
 
 Pins (tests/test_oracle_moe.py): hand-worked RMSNorm values
 (tests/golden/rmsnorm_cases.txt), silu closed forms, brute-force top-k over
-all k-subsets on small E, an expert built from hand-chosen bytes and codes
-whose result is worked out by hand, and, for the composed step, three
-invariants: the one-token / one-expert reduction, identical routed experts
-(the picks' weights sum to one: out = bf16(y + y_shared) whatever is
+all k-subsets on small E, hand rows for ``topk_gaps`` (a close pair inside
+the top k, a close pair at the k / k+1 boundary, a close pair below it that
+must not count), an expert built from hand-chosen bytes and codes whose
+result is worked out by hand, a hand ``combine`` on two tokens with unequal
+weights, and, for the composed step, a hand-built layer whose two picked
+experts output different constants with unequal weights (and its mirror, the
+constants swapped), which fixes the pairing of weight j with pick j; plus
+three invariants: the one-token / one-expert reduction, identical routed
+experts (the picks' weights sum to one: out = bf16(y + y_shared) whatever is
 picked) and token-permutation invariance. The composed step has no worked
 example on the pages: beyond what those pins and invariants fix, its
-end-to-end numbers are "parity unpinned".
+end-to-end numbers on random layers are "parity unpinned".
 """
 
 from __future__ import annotations
@@ -214,17 +219,15 @@ def decode_step(x, norm_w, gate_w, bias, topk: int, get_expert, get_shared,
     out = np.full((m, hdim), np.nan)
     if rows:
         y_routed = np.zeros((m, topk, hdim))
-        y_shared = np.zeros((m, hdim))
         wanted = sorted({int(e) for t in rows for e in rt.ids[t]})
         for e in wanted:
-            ew = get_expert(e)
-            for t in rows:
-                for j in range(topk):
-                    if rt.ids[t, j] == e:
-                        y_routed[t, j] = expert(x_hat[t : t + 1], ew)[0][0]
-        sh = get_shared()
-        for t in rows:
-            y_shared[t] = expert(x_hat[t : t + 1], sh)[0][0]
-        res = combine(y_routed[rows], rt.weights[rows], y_shared[rows])
-        out[rows] = res
+            # every (token, pick) that chose expert e, in one call: each output
+            # row of ``expert`` depends on its own input row only (per-row
+            # contraction, per-row requant along I)
+            picks = [(t, j) for t in rows for j in range(topk) if rt.ids[t, j] == e]
+            y = expert(x_hat[[t for t, _ in picks]], get_expert(e))[0]
+            for (t, j), y_tj in zip(picks, y):
+                y_routed[t, j] = y_tj
+        y_shared = expert(x_hat[rows], get_shared())[0]
+        out[rows] = combine(y_routed[rows], rt.weights[rows], y_shared)
     return StepResult(normed=normed, x8=x8, codes=codes, routing=rt, out=out)

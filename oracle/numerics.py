@@ -64,19 +64,6 @@ def bf16_rne(v):
     return out
 
 
-def bf16_bits_to_f64(bits):
-    """uint16 bf16 bit patterns -> float64 values (exact)."""
-    b = np.asarray(bits, dtype=np.uint32) << 16
-    return b.view(np.float32).astype(np.float64) if b.ndim else \
-        np.array([b], dtype=np.uint32).view(np.float32).astype(np.float64)[0]
-
-
-def f64_to_bf16_bits(v):
-    """bf16-exact float64 value(s) -> uint16 bit patterns."""
-    f = np.asarray(v, dtype=np.float64).astype(np.float32)
-    return (f.view(np.uint32) >> 16).astype(np.uint16)
-
-
 def _e4m3_value(byte: int) -> float:
     """Value of one E4M3 byte from the OCP FP8 E4M3FN definition."""
     s = -1.0 if byte & 0x80 else 1.0

@@ -267,3 +267,81 @@ def test_step_token_subset_matches_full():
                            tokens=[2])
     assert np.array_equal(full.out[2], part.out[2])
     assert np.all(np.isnan(part.out[[0, 1, 3]]))
+
+
+def test_topk_gaps_hand_rows():
+    # the smallest gap among the k + 1 largest choices; the rows are shuffled
+    # too (the function must sort them first)
+    k = 3
+    rows = np.array([
+        [0.9, 0.6, 0.3, 0.0, -0.3],        # clean: every gap is 0.3
+        [0.9, 0.5, 0.4995, 0.1, 0.0],      # a close pair inside the top k (picks 2 and 3)
+        [0.9, 0.6, 0.3, 0.2995, 0.0],      # a close pair at the boundary (pick k vs k + 1)
+        [0.9, 0.6, 0.3, 0.0, -0.0004],     # a close pair below the k + 1 largest: ignored
+        [0.9, 0.6, 0.6, 0.0, -0.3],        # a tie inside the top k: gap 0
+    ])
+    want = np.array([0.3, 0.0005, 0.0005, 0.3, 0.0])
+    np.testing.assert_allclose(moe.topk_gaps(rows, k), want, rtol=0, atol=1e-12)
+    perm = [3, 0, 4, 2, 1]
+    np.testing.assert_allclose(moe.topk_gaps(rows[:, perm], k), want, rtol=0, atol=1e-12)
+    # k = 1: only the gap between the largest and the second largest counts
+    np.testing.assert_allclose(moe.topk_gaps(rows, 1), [0.3, 0.4, 0.3, 0.3, 0.3],
+                               rtol=0, atol=1e-12)
+
+
+def test_combine_hand_two_tokens():
+    # token 0: picks output 1 and 3 with weights 0.25, 0.75 and the shared
+    # expert 0.5: 0.25 + 2.25 + 0.5 = 3.0; token 1 the picks swapped:
+    # 0.75 + 0.75 + 0.5 = 2.0; token 2: 0.5 * 1 + 0.5 * 5 + 2^-7 = 3 + 2^-7
+    # lies halfway between the bf16 neighbours 3 and 3 + 2^-6 and rounds to
+    # the even one, 3.0
+    h = 4
+    y = np.zeros((3, 2, h))
+    y[0, 0], y[0, 1] = 1.0, 3.0
+    y[1, 0], y[1, 1] = 3.0, 1.0
+    y[2, 0], y[2, 1] = 1.0, 5.0
+    w = np.array([[0.25, 0.75], [0.25, 0.75], [0.5, 0.5]])
+    ysh = np.array([[0.5] * h, [0.5] * h, [2.0 ** -7] * h])
+    out = moe.combine(y, w, ysh)
+    assert np.array_equal(out, np.array([[3.0] * h, [2.0] * h, [3.0] * h]))
+
+
+def _const_expert(y_byte: int, y_code: int) -> moe.ExpertWeights:
+    """H = I = 32 expert whose output is a constant on the all-ones x_hat row:
+    gate rows 1.0 * 2^1 -> g = 32 * 2 = 64 and silu(64) = 64 in float64; up
+    rows 1.0 * 2^-11 -> u = 2^-6, so h = 1 (code 119, byte 0x78, exact); the
+    w2 entries are y_byte * 2^(y_code - 127), so y = 32 * that value."""
+    w13 = np.full((64, 32), 0x38, np.uint8)            # E4M3 1.0
+    w13_s = np.array([[128], [116]], np.uint8)         # gate block x2, up block x2^-11
+    w2 = np.full((32, 32), y_byte, np.uint8)
+    w2_s = np.array([[y_code]], np.uint8)
+    return moe.ExpertWeights.from_quantised(w13, w13_s, w2, w2_s)
+
+
+def test_step_pairs_weights_with_their_picks():
+    # normed = 1 (x = 1, w = 1, eps = 0), so the logits are the gate rows'
+    # sums: 0, ln 3, -ln 3, 0 -> scores 1/2, 3/4, 1/4, 1/2; the bias makes the
+    # choices -0.5, 0.75, 0.85, -0.5, so k = 2 picks [2, 1] with weights
+    # 1/4 and 3/4. Expert 1 outputs 1 (0x38 * 2^-5 * 32), expert 2 outputs 3
+    # (0x3C = 1.5, * 2^-4 * 32), the shared expert 0.5 (0x38 * 2^-6 * 32), the
+    # unpicked ones 32: out = 1/4 * 3 + 3/4 * 1 + 1/2 = 2. Pairing weight j
+    # with another pick gives 3; the mirror case (the two outputs swapped)
+    # gives 3 where a wrong pairing gives 2.
+    h = 32
+    ln3 = math.log(3.0)
+    gate_w = np.zeros((4, h))
+    gate_w[1] = ln3 / h
+    gate_w[2] = -ln3 / h
+    bias = np.array([-1.0, 0.0, 0.6, -1.0])
+    x = np.ones((1, h))
+    other = _const_expert(0x38, 127)
+    one, three = _const_expert(0x38, 122), _const_expert(0x3C, 123)
+    half = _const_expert(0x38, 121)
+    for e1, e2, want in ((one, three, 2.0), (three, one, 3.0)):
+        experts = {0: other, 1: e1, 2: e2, 3: other}
+        res = moe.decode_step(x, np.ones(h), gate_w, bias, 2, lambda e: experts[e],
+                              lambda: half, eps=0.0)
+        assert np.array_equal(res.normed, np.ones((1, h)))
+        assert res.routing.ids.tolist() == [[2, 1]]
+        np.testing.assert_allclose(res.routing.weights, [[0.25, 0.75]], rtol=1e-14)
+        assert np.array_equal(res.out, np.full((1, h), want)), (want, res.out[0, :4])
