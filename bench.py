@@ -10,8 +10,9 @@ resident in HBM; L2 is flushed (a 512 MB write) before every timed step.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl mine|reference] [--no-sweep]
 
---impl reference times the CPU oracle (the reference arm of this build) on a
-bounded sample of the same workload and scales it to one step. Under torchrun
+--impl reference times the CPU oracle (the reference arm of this build):
+complete steps of the same workload, as many of the requested ones as fit a
+fixed budget (it prints the counts it ran). Under torchrun
 (N > 1) each rank runs an independent replica of the step (the layer does not
 shard on one box); rank 0 prints.
 """
@@ -49,7 +50,7 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-experts", type=int, default=4,
-                    help="experts the CPU baseline evaluates per sample")
+                    help="experts of the CPU baseline's sampled estimate (0: none)")
     return ap.parse_args()
 
 
@@ -147,6 +148,17 @@ class Clocks:
         busy = [s for s in sm if s > 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def base_config(wl, unique: int) -> dict:
+    """The workload's keys, the same in both arms' lines."""
+    from mxfp8_moe_decode_gb300 import workloads as W
+
+    d = wl.dims
+    return {"workload": wl.name, "desc": wl.note, "M": wl.tokens, "hidden": d.hidden,
+            "experts": d.experts, "topk": d.topk, "inter": d.inter, "routed_format": d.routed,
+            "shared_experts": 1, "unique_routed_experts": unique,
+            "alg_bytes_per_step": W.algorithmic_bytes(d, unique)}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -359,28 +371,51 @@ def run_gpu(args):
                 if peaks["source"] == "measured" else "fallback 6.8 TB/s"}
     step_gbs = alg / (us_step * 1e-6) / 1e9 if world == 1 else None
 
-    # end to end: host (pinned) x -> device, the step, device out -> host
+    # end to end: host (pinned) x -> device, the step, device out -> host,
+    # on one stream between two events, L2 flushed before each step. Two legs:
+    # the public call (MoeDecode.step -> moe_decode_step, launches enqueued
+    # by the host every step) and the step's CUDA graph replayed between the
+    # same copies.
     xh = x.cpu().pin_memory()
     oh = torch.empty_like(xh).pin_memory()
     cur = torch.cuda.current_stream(dev)
     xd = x  # the graph reads x's storage
-    for _ in range(args.warmup):
-        xd.copy_(xh, non_blocking=True)
+    out_call = torch.empty_like(x)
+
+    def e2e_leg(one_step) -> float:
+        for _ in range(args.warmup):
+            xd.copy_(xh, non_blocking=True)
+            one_step()
+            oh.copy_(out_call, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t = []
+        for _ in range(args.steps):
+            flush()
+            e0.record(cur)
+            xd.copy_(xh, non_blocking=True)
+            one_step()
+            oh.copy_(out_call, non_blocking=True)
+            e1.record(cur)
+            e1.synchronize()
+            t.append(e0.elapsed_time(e1))
+        return statistics.mean(t) * 1e3
+
+    e2e_us = e2e_leg(lambda: layer.step(xd, out=out_call))
+    if layer.status() != 0:
+        raise RuntimeError(f"device status {layer.status()}")
+    got_call = out_call.clone()
+
+    def graph_step():
         graph.replay()
-        oh.copy_(out, non_blocking=True)
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e = []
-    for _ in range(args.steps):
-        flush()
-        e0.record(cur)
-        xd.copy_(xh, non_blocking=True)
-        graph.replay()
-        oh.copy_(out, non_blocking=True)
-        e1.record(cur)
-        e1.synchronize()
-        e2e.append(e0.elapsed_time(e1))
-    e2e_us = statistics.mean(e2e) * 1e3
+        out_call.copy_(out, non_blocking=True)
+
+    e2e_graph_us = e2e_leg(graph_step)
+    if not torch.equal(out_call, got_call):
+        raise RuntimeError("graph replay and the direct call disagree")
+    cpu_ref = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu_ref = cpu_baseline(wl, ew, unique, args.cpu_experts)
 
     sweep, next_rows = {}, {}
     if not args.no_sweep and world == 1:
@@ -430,10 +465,8 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "e4m3 (mxfp8 block-scaled MMA, fp32 accumulate)",
         "data": "synthetic (seeded; random-init weights of the layer's shapes)",
-        "config": {"workload": wl.name, "desc": wl.note, "M": wl.tokens, "hidden": d.hidden,
-                   "experts": d.experts, "topk": d.topk, "inter": d.inter,
-                   "shared_experts": 1, "unique_routed_experts": unique,
-                   "alg_bytes_per_step": alg, "step_gbs": round(step_gbs, 1) if step_gbs else None,
+        "config": {**base_config(wl, unique),
+                   "step_gbs": round(step_gbs, 1) if step_gbs else None,
                    "step_frac_of_peak": round(step_gbs / peaks["hbm_gbs"], 4) if step_gbs else None,
                    "step_frac_of_8tbs": round(step_gbs / NOMINAL_GBS, 4) if step_gbs else None,
                    "median_us_per_step": round(statistics.median(step_ms) * 1e3, 3),
@@ -447,7 +480,14 @@ def run_gpu(args):
         "roofline": roofline,
         "kernel_us": kernel_table(names, kmean, launches_per_step),
         "e2e": {"value": round(e2e_us, 3), "unit": "us",
-                "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2},
+                "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2,
+                "method": "per step: pinned host x -> device copy, the public call "
+                          "(MoeDecode.step -> moe_decode_step, its launches enqueued by the "
+                          "host), device out -> pinned host copy; one stream, CUDA events "
+                          "around the three, L2 flushed before each step",
+                "graph_replay_value": round(e2e_graph_us, 3),
+                "graph_replay_method": "the same copies around a replay of the step's "
+                                       "CUDA graph (captured from the same call)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -455,8 +495,8 @@ def run_gpu(args):
         line["sweep"] = sweep
     if next_rows:
         line["next_rows"] = next_rows
-    if rank == 0 and world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_experts, unique)
+    if cpu_ref is not None:
+        line["cpu_baseline"] = cpu_ref
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -485,84 +525,143 @@ def blas_threads() -> str:
     return "library default"
 
 
-def cpu_baseline(wl, n_experts: int, unique: int | None = None, repeats: int = 1) -> dict:
-    """The oracle, as it stands, on the host cores: the seam and router on all M
-    rows plus the expert path of a sample of the touched experts (dequantise +
-    per-token contraction), scaled to the step's unique + shared experts."""
-    import numpy as np
-    import torch
+def _host_expert_getters(wl, ew_host):
+    """Oracle accessors over host copies of the layer's weight tensors."""
+    from oracle import moe as O
 
+    make = O.ExpertWeights.from_fp4 if wl.dims.routed == "e2m1" else O.ExpertWeights.from_quantised
+
+    def get_expert(e):
+        return make(ew_host["w13"][e].numpy(), ew_host["w13_s"][e].numpy(),
+                    ew_host["w2"][e].numpy(), ew_host["w2_s"][e].numpy())
+
+    def get_shared():
+        return O.ExpertWeights.from_quantised(ew_host["sw13"].numpy(), ew_host["sw13_s"].numpy(),
+                                              ew_host["sw2"].numpy(), ew_host["sw2_s"].numpy())
+
+    return get_expert, get_shared
+
+
+def oracle_step(wl, ew_host):
+    """One complete oracle step of the workload on the host: the seam and the
+    router on all M rows, every touched routed expert and the shared expert
+    over their rows, the combine. Returns (seconds, unique routed experts)."""
     from mxfp8_moe_decode_gb300 import workloads as W
     from oracle import moe as O
-    from oracle.mx import dequant_rows
 
     d = wl.dims
     ri = W.router_inputs(wl)
-    x = W.token_rows(wl)
     f64 = lambda t: t.float().double().numpy()  # noqa: E731
+    x, nw, gw, b = f64(W.token_rows(wl)), f64(ri["norm_w"]), f64(ri["gate_w"]), f64(ri["bias"])
+    get_expert, get_shared = _host_expert_getters(wl, ew_host)
     t0 = time.perf_counter()
-    normed = O.rmsnorm(f64(x), f64(ri["norm_w"]), d.eps)
-    x8, codes = O.seam_quant(normed)
-    rt = O.router(normed, f64(ri["gate_w"]), f64(ri["bias"]), d.topk)
-    x_hat = dequant_rows(x8, codes)
-    t_front = time.perf_counter() - t0
-    ids = np.unique(rt.ids)
-    u = len(ids) if unique is None else unique
-    sample = [int(e) for e in ids[:n_experts]]
-    key = (wl.name, tuple(sample))
-    if key not in _CPU_WEIGHTS:
-        _CPU_WEIGHTS.clear()
-        _CPU_WEIGHTS[key] = W.expert_weights(wl, device="cpu", experts=sample)
-    ew = _CPU_WEIGHTS[key]
-    t_exp = 0.0
-    for e in sample:
-        tok = [t for t in range(x.shape[0]) if e in rt.ids[t]]
-        t1 = time.perf_counter()
-        w = O.ExpertWeights.from_quantised(ew["w13"][e].numpy(), ew["w13_s"][e].numpy(),
-                                           ew["w2"][e].numpy(), ew["w2_s"][e].numpy())
-        O.expert(x_hat[tok], w)
-        t_exp += time.perf_counter() - t1
-    per_expert = t_exp / max(1, len(sample))
-    est_s = t_front + per_expert * (u + 1)
-    return {"value": round(est_s * 1e6, 1), "unit": "us", "cores": len(os.sched_getaffinity(0)),
+    res = O.decode_step(x, nw, gw, b, d.topk, get_expert, get_shared, d.eps)
+    dt = time.perf_counter() - t0
+    return dt, len(set(res.routing.ids.reshape(-1).tolist()))
+
+
+def cpu_baseline(wl, ew, unique: int, n_sample: int = 4) -> dict:
+    """The oracle, as it stands, on the host cores: one complete step of the
+    workload (value), on host copies of the weights the GPU step ran on (the
+    copies are not timed); beside it, the older sampled estimate (the expert
+    path of n_sample touched experts scaled to all of them), labelled."""
+    ew_host = {k: v.cpu() for k, v in ew.items()}
+    dt, u = oracle_step(wl, ew_host)
+    line = {"value": round(dt * 1e6, 1), "unit": "us", "cores": len(os.sched_getaffinity(0)),
             "blas_threads": blas_threads(), "kind": "oracle",
-            "sample": f"{wl.name}: seam + router on all {x.shape[0]} rows, then the fp64 expert "
-                      f"path of {len(sample)} of the {u} touched routed experts "
-                      f"({per_expert:.2f} s each), scaled to {u} + 1 shared experts"}
+            "sample": f"one complete oracle step of {wl.name}: {wl.tokens} rows, {u} touched "
+                      f"routed experts + the shared one, fp64 (timed once; no scaling)"}
+    if u != unique:
+        line["note"] = f"oracle touched {u} routed experts, the GPU step {unique}"
+    if n_sample > 0:
+        # the older estimate: the expert path (dequantise + contraction) of the
+        # first n_sample touched experts over their own rows, scaled to all
+        import numpy as np
+
+        from mxfp8_moe_decode_gb300 import workloads as W
+        from oracle import moe as O
+        from oracle.mx import dequant_rows
+
+        d = wl.dims
+        ri = W.router_inputs(wl)
+        f64 = lambda t: t.float().double().numpy()  # noqa: E731
+        x = f64(W.token_rows(wl))
+        normed = O.rmsnorm(x, f64(ri["norm_w"]), d.eps)
+        x_hat = dequant_rows(*O.seam_quant(normed))
+        rt = O.router(normed, f64(ri["gate_w"]), f64(ri["bias"]), d.topk)
+        get_expert, _ = _host_expert_getters(wl, ew_host)
+        sample = [int(e) for e in np.unique(rt.ids)[:n_sample]]
+        t = 0.0
+        for e in sample:
+            rows = [r for r in range(x.shape[0]) if e in rt.ids[r]]
+            t1 = time.perf_counter()
+            O.expert(x_hat[rows], get_expert(e))
+            t += time.perf_counter() - t1
+        line["sampled_estimate_us"] = round(t / max(1, len(sample)) * (unique + 1) * 1e6, 1)
+        line["sampled_estimate"] = (f"expert path of {len(sample)} touched experts over their "
+                                    f"rows, scaled to {unique} + 1 experts (an estimate)")
+    del ew_host
+    return line
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, complete steps of
+    the same workload. Each step takes seconds to tens of seconds, so the arm
+    runs as many of the requested steps as fit a fixed budget (at least one,
+    after one warm-up step) and prints the counts it ran."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import torch
+
     from mxfp8_moe_decode_gb300 import workloads as W
 
     wl = W.WORKLOADS[args.workload]
-    vals = []
-    info = None
-    for i in range(args.warmup + args.steps):
-        info = cpu_baseline(wl, 1)
-        if i >= args.warmup:
-            vals.append(info["value"])
-    v = statistics.mean(vals)
+    # inputs: the weights drawn exactly as the GPU arm draws them (on the GPU
+    # when there is one), then held in host memory; not timed
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    ew = W.expert_weights(wl, device=dev)
+    ew_host = {k: v.cpu() for k, v in ew.items()}
+    del ew
+    if dev != "cpu":
+        torch.cuda.empty_cache()
+    budget_s = float(os.environ.get("MOE_REFERENCE_BUDGET_S", "150"))
+    warm = 0
+    t_warm = None
+    if args.warmup > 0:
+        t_warm, _ = oracle_step(wl, ew_host)
+        warm = 1
+    n = args.steps
+    if t_warm is not None:
+        n = max(1, min(args.steps, int(budget_s // max(t_warm, 1e-9))))
+    vals, unique = [], 0
+    for _ in range(n):
+        dt, unique = oracle_step(wl, ew_host)
+        vals.append(dt)
+    v = statistics.mean(vals) * 1e6
     line = {
         "impl": "reference",
         "metric": METRIC,
         "value": round(v, 1),
         "unit": "us",
         "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+        "steps": n,
+        "warmup": warm,
+        "requested": {"steps": args.steps, "warmup": args.warmup},
         "ms_per_step": round(v / 1e3, 3),
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
-        "data": "synthetic (seeded)",
-        "config": {"workload": wl.name, "desc": wl.note, "M": wl.tokens},
-        "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": info["cores"],
-                         "kind": "oracle", "sample": info["sample"]},
+        "data": "synthetic (seeded; the same draws as the GPU arm)",
+        "config": base_config(wl, unique),
+        "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": len(os.sched_getaffinity(0)),
+                         "blas_threads": blas_threads(), "kind": "oracle",
+                         "sample": f"complete oracle steps of {wl.name} ({wl.tokens} rows, "
+                                   f"{unique} routed + 1 shared experts, fp64); {warm} warm-up "
+                                   f"and {n} timed of the {args.steps} requested, as many as "
+                                   f"fit {budget_s:.0f} s"},
         "e2e": {"value": round(v, 1), "unit": "us", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

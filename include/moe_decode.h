@@ -152,9 +152,16 @@ typedef struct moe_handle moe_handle;
  * MOE_ERR_ALIGN (a weight pointer not 16-byte aligned, or with
  * MOE_ROUTED_E2M1 the routed w13 / w2 not 32-byte aligned), MOE_ERR_DEVICE,
  * MOE_ERR_CUDA, MOE_ERR_CAPTURE (the legacy stream of `device` is being
- * captured: creation allocates and synchronises). With MOE_ROUTED_E2M1 the
+ * captured: creation allocates and synchronises), and MOE_ERR_UNSUPPORTED
+ * also when one CTA of the expert kernel (288 threads, about 220 KB of shared
+ * memory) cannot be resident on an SM of this device. With MOE_ROUTED_E2M1 the
  * handle also holds the routed experts' per-row scale codes regrouped for the
  * tensor cores (as many bytes as w13_s and w2_s).
+ *
+ * The expert kernel launches one CTA per SM of the device and hands its tasks
+ * out in order from a counter: its progress does not depend on how many of
+ * those CTAs are resident at once, so kernels running beside it, or a context
+ * limited to fewer SMs, make a step slower but never stall it.
  */
 int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_handle** out);
 
@@ -180,8 +187,24 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
  */
 int moe_status(moe_handle* h);
 
-/* Resets the device-side error word (synchronous). MOE_ERR_CAPTURE during capture. */
+/* Resets the device-side error word (synchronous). MOE_ERR_CAPTURE during capture.
+ * moe_status, moe_clear_status, moe_last_unique_experts and moe_destroy work on
+ * the handle's device and leave the calling thread's current device as it was. */
 int moe_clear_status(moe_handle* h);
+
+/*
+ * Test hook for the device-side timeout path (off by default; the source
+ * pages have no counterpart). While unit >= 0, the steps enqueued on this
+ * handle never report the w13 tiles of the expert kernel's unit `unit` as
+ * done (unit 0 is the shared expert, present in every step), so each w2 task
+ * of that unit waits until its bounded wait (1 s) expires: the CTA records
+ * MOE_ERR_TIMEOUT in the error word, lets its copies and MMAs in flight
+ * complete, frees its tensor memory and exits, and the step's output is
+ * unspecified. No memory fault and no hang: the stream completes. unit = -1
+ * turns the hook off. Errors: MOE_ERR_ARG (null handle), MOE_ERR_RANGE (unit
+ * < -1 or beyond the handle's unit capacity).
+ */
+int moe_test_withhold_ready(moe_handle* h, int unit);
 
 /*
  * Number of distinct routed experts the last completed step used (synchronous
@@ -285,16 +308,33 @@ void moe_destroy(moe_handle* h);
  *
  * The first call on a device (with that device current) looks up the array's
  * device address and sets the kernel's shared-memory limit; make that first
- * call before any stream capture. Each call enqueues a memset of the array's
- * counters and two kernels on `stream` (void* holding a cudaStream_t). All
- * calls share the one array, which keeps the last call's contents: calls whose
- * work overlaps on the GPU (different streams, or concurrent host threads
- * without ordering) race on it and must be serialised by the caller.
+ * call before any stream capture. The address is kept until the process
+ * exits: calls after a cudaDeviceReset of that device are not supported. Each
+ * call enqueues a memset of the array's counters and two kernels on `stream`
+ * (void* holding a cudaStream_t). All calls share the one array, which keeps
+ * the last call's contents: calls whose work overlaps on the GPU (different
+ * streams, or concurrent host threads without ordering) race on it and must
+ * be serialised by the caller.
+ *
+ * Device-side errors are not returned by the call (it only enqueues): read
+ * them with moe_route_static_status. Rows whose scores are not finite (NaN or
+ * infinite inputs) give unspecified ids and NaN weights and no error.
  */
 #define MOE_ROUTE_STATIC_SCRATCH_BYTES (256 * 1024)
 int moe_route_static(const void* normed, const void* gate_w, const float* bias, int M,
                      int hidden, int experts, int topk, int32_t* topk_ids, float* topk_w,
                      void* stream);
+
+/*
+ * Device-side status of the moe_route_static calls enqueued on the current
+ * device (void* stream holding a cudaStream_t): waits for `stream`, then
+ * reads the array's error word, which each moe_route_static call clears when
+ * it starts. Returns MOE_OK, MOE_ERR_TIMEOUT (a kernel gave up a bounded wait:
+ * that call's outputs are unspecified), MOE_ERR_CAPTURE (the stream is being
+ * captured: this call synchronises), MOE_ERR_CUDA, or MOE_OK if no call has
+ * run on the device yet. Allocates nothing.
+ */
+int moe_route_static_status(void* stream);
 
 /*
  * Attention-seam MXFP8 ("vllm.models.deepseek_v41.amd.mono.layer", store_x8:

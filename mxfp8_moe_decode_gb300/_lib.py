@@ -89,6 +89,12 @@ def lib() -> ctypes.CDLL:
     L.moe_destroy.restype = None
     L.moe_attn_seam_x8.argtypes = [vp, vp, ip, ip, ctypes.c_float, vp, vp, vp, vp]
     L.moe_attn_seam_x8.restype = ip
+    L.moe_test_withhold_ready.argtypes = [vp, ip]
+    L.moe_test_withhold_ready.restype = ip
+    L.moe_route_static.argtypes = [vp, vp, vp, ip, ip, ip, ip, vp, vp, vp]
+    L.moe_route_static.restype = ip
+    L.moe_route_static_status.argtypes = [vp]
+    L.moe_route_static_status.restype = ip
     _LIB = L
     return L
 

@@ -200,6 +200,12 @@ class MoeDecode:
     def clear_status(self) -> int:
         return _lib.lib().moe_clear_status(self._h)
 
+    def test_withhold_ready(self, unit: int) -> None:
+        """Test hook (``moe_test_withhold_ready``): the expert kernel's unit
+        ``unit`` never reports its w13 tiles done, so the step's bounded waits
+        expire (status MOE_ERR_TIMEOUT); -1 turns it off."""
+        check(_lib.lib().moe_test_withhold_ready(self._h, unit), "test_withhold_ready")
+
     def step_launches(self, m: int) -> int:
         """Kernels one step of m tokens launches."""
         return _lib.lib().moe_step_launches(self._h, m)

@@ -44,6 +44,7 @@ struct moe_handle {
   cudaEvent_t events[16];
   int n_events;
   cudaStream_t last_stream;
+  int withhold_unit;  // test hook (moe_test_withhold_ready): -1 = off
 };
 
 namespace {
@@ -158,6 +159,28 @@ int validate_weights(const moe_weights* w, int routed_format) {
 // its K-slice of the normed rows (whole 32-column groups).
 bool seam_fused(const moe_handle* h, int M) { return M <= kSeamFuseMaxM && h->hs % 32 == 0; }
 
+// Makes a device current for the lifetime of the object and gives the caller
+// back its own current device afterwards (host-side calls that synchronise or
+// copy on the handle's device leave no trace in the calling thread's state).
+class DeviceScope {
+ public:
+  explicit DeviceScope(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) {
+      cudaGetLastError();
+      prev_ = -1;
+    }
+    ok_ = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceScope() {
+    if (prev_ >= 0) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = false;
+};
+
 }  // namespace
 
 extern "C" {
@@ -237,6 +260,17 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MOE_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_DEVICE;
   if (!get_encode_fn()) return MOE_ERR_CUDA;
+  // one expert CTA (288 threads, ~220 KB of shared memory) must fit an SM
+  {
+    int per_sm = 0;
+    const cudaError_t e =
+        expert_occupancy(cfg->routed_format == MOE_ROUTED_E2M1 ? 1 : 0, &per_sm);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
+  }
 
   moe_handle* h = new (std::nothrow) moe_handle();
   if (!h) return MOE_ERR_CUDA;
@@ -245,6 +279,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->w = *w;
   h->device = device;
   h->num_sms = prop.multiProcessorCount;
+  h->withhold_unit = -1;
 
   const int H = cfg->hidden, E = cfg->experts, K = cfg->topk, I = cfg->inter;
   const int Mx = cfg->max_tokens;
@@ -365,6 +400,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   pe.g2 = g2;
   pe.units_max = h->units_max;
   pe.rows_max = h->rows_max;
+  pe.withhold_unit = -1;
   // w13 as [2E halves][I rows][H]: one box = 64 gate rows over the 64 matching up rows
   const WeightType wt = fp4 ? kE2M1Map : kE4M3Map;
   bool ok = encode_planes(&pe.tm_w13, w->w13, H, I, 2ull * E, 64, 2, wt) &&
@@ -462,6 +498,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   // step's partial rows, which start at zero
   const int g2 = h->cfg.inter / 128;
   const bool split = M <= kW2SplitMaxM && g2 >= 4 && g2 % 2 == 0;
+  rp.err = h->counters + kCtrErr;
   rp.zero_rows = split ? h->part : nullptr;
   rp.zero_n = split ? static_cast<size_t>(M) * (K + 1) * H : 0;
   const bool pf = M <= kPrefetchMaxM;
@@ -513,6 +550,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   ExpertParams pe = h->pe;
   pe.M = M;
   pe.K = K;
+  pe.withhold_unit = h->withhold_unit;
   pe.split_tiles = split ? h->num_sms : 0;
   if (err == cudaSuccess) err = launch_experts(pe, h->num_sms, st);
   mark(4);
@@ -529,7 +567,8 @@ int moe_status(moe_handle* h) {
     return MOE_ERR_CAPTURE;
   }
   if (cs != cudaStreamCaptureStatusNone) return MOE_ERR_CAPTURE;
-  if (cudaSetDevice(h->device) != cudaSuccess) return MOE_ERR_CUDA;
+  DeviceScope scope(h->device);
+  if (!scope.ok()) return MOE_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   int word = 0;
   if (cudaMemcpy(&word, h->counters + kCtrErr, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -547,7 +586,8 @@ int moe_clear_status(moe_handle* h) {
     cudaGetLastError();
     return MOE_ERR_CAPTURE;
   }
-  if (cudaSetDevice(h->device) != cudaSuccess) return MOE_ERR_CUDA;
+  DeviceScope scope(h->device);
+  if (!scope.ok()) return MOE_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(h->counters + kCtrErr, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaDeviceSynchronize() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -555,12 +595,20 @@ int moe_clear_status(moe_handle* h) {
 
 int moe_last_unique_experts(moe_handle* h, int* unique_routed) {
   if (!h || !unique_routed) return MOE_ERR_ARG;
-  if (cudaSetDevice(h->device) != cudaSuccess) return MOE_ERR_CUDA;
+  DeviceScope scope(h->device);
+  if (!scope.ok()) return MOE_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   int v = 0;
   if (cudaMemcpy(&v, h->counters + kCtrRouted, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
   *unique_routed = v;
+  return MOE_OK;
+}
+
+int moe_test_withhold_ready(moe_handle* h, int unit) {
+  if (!h) return MOE_ERR_ARG;
+  if (unit < -1 || unit >= h->units_max) return MOE_ERR_RANGE;
+  h->withhold_unit = unit;
   return MOE_OK;
 }
 
@@ -581,9 +629,12 @@ int moe_set_timing_events(moe_handle* h, void* const* events, int n) {
 
 void moe_destroy(moe_handle* h) {
   if (!h) return;
-  if (cudaSetDevice(h->device) == cudaSuccess) {
-    cudaDeviceSynchronize();
-    cudaFree(h->scratch);
+  {
+    DeviceScope scope(h->device);
+    if (scope.ok()) {
+      cudaDeviceSynchronize();
+      cudaFree(h->scratch);
+    }
   }
   cudaGetLastError();
   delete h;

@@ -22,10 +22,11 @@
 //    K = I. Its weight stages are issued at once; its activation stages wait
 //    (bounded) until all w13 tiles of the unit are done. Epilogue: fp32 rows
 //    of y for the combine.
-// Tasks are handed out in that order from a global counter. Every w13 task
-// is handed out before any w2 task, to a CTA that finishes it without waiting
-// on anything, so the readiness waits always end (all CTAs of the grid, one
-// per SM, are resident).
+// Tasks are handed out in that order from a global counter, every CTA's
+// first task included. Every w13 task is handed out before any w2 task, to a
+// CTA that is running and finishes it without waiting on anything, so the
+// readiness waits always end, however many of the grid's CTAs are resident
+// at once.
 //
 // Per CTA (one per SM, 288 threads):
 //  warp 8 lane 0, the scheduler, claims the CTA's tasks one ahead of the
@@ -407,6 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           const uint32_t round = it / kStages;
           if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty[s]), (round & 1) ^ 1, abort,
                               kWaitLimitNs)) {
+            // the held-back activation copies of the stages already expected
+            // still go out, so that each of those stages completes before exit
+            for (int q = 0; q < n_pending; ++q)
+              issue_b(g - n_pending + q, static_cast<int>((first_pending + q) % kStages));
             ok = false;
             break;
           }
@@ -670,24 +675,33 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         // waits for the SM's copies in flight, so there is just one)
         asm volatile("fence.proxy.async.global;" ::: "memory");
         epi_bar();
-        if (threadIdx.x == 128)
+        if (threadIdx.x == 128 && k.u != p.withhold_unit)
           asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.ready + k.u) : "memory");
       }
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ scheduler
-    // The shared expert is unit 0 in every step, with the fixed entry (E,
-    // first row M K, M rows), and its x panels come from the seam, two kernels
-    // back (complete once this grid runs: the top-k kernel lets it launch only
-    // after its own wait). So its w13 tiles need no routing: CTA b < t13 posts
-    // tile b at once, and it streams while the top-k kernel finishes.
-    const int grid = static_cast<int>(gridDim.x);
-    const bool pre = static_cast<int>(blockIdx.x) < p.t13;
+    // Every task comes from the step's counter, the first one included, so a
+    // CTA that starts late (fewer SMs free than the grid has CTAs) never holds
+    // back a task that a resident CTA waits for: w13 tasks precede every w2
+    // task in the claim order, and a CTA only claims its next task while the
+    // current one runs. The router zeroed the counter two kernels back
+    // (complete once this grid runs: the top-k kernel lets it launch only
+    // after its own wait), so the first claim can go out before this grid's
+    // own dependency wait. The shared expert is unit 0 in every step, with the
+    // fixed entry (E, first row M K, M rows), and its x panels come from the
+    // seam, also two kernels back: a first claim below t13 is one of its w13
+    // tiles, which needs no routing and is posted at once, so it streams while
+    // the top-k kernel finishes.
+    int first_task = 0;
+    if (lane == 0) first_task = atomicAdd(p.task_ctr, 1);
+    first_task = __shfl_sync(0xffffffffu, first_task, 0);
+    const bool pre = first_task < p.t13;
     bool pre_ok = true;
     if (pre && lane == 0) {
-      const Task k0 = {0, 0, static_cast<int>(blockIdx.x), 0, p.g13, 0};
-      pre_ok = post_task(bars, misc, 0, static_cast<int>(blockIdx.x),
-                         make_int4(p.E, p.M * p.K, p.M, 0), pack_task(k0), abort);
+      const Task k0 = {0, 0, first_task, 0, p.g13, 0};
+      pre_ok = post_task(bars, misc, 0, first_task, make_int4(p.E, p.M * p.K, p.M, 0),
+                         pack_task(k0), abort);
       if (pre_ok) st_release_cta(&misc->ready_seq, 0);
     }
     // The routing (row counts) and the routed experts' x panels come from the
@@ -763,25 +777,24 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     const int w2full = n2 > p.split_tiles ? n2 - p.split_tiles : 0;  // the rest go in halves
     const int ntasks = n13 + w2full + 2 * (n2 - w2full);
 
-    // Claims the CTA's tasks, one ahead of the producer: the first is the
-    // CTA's index, each later one comes from the counter (offset by the grid)
+    // Claims the CTA's tasks, one ahead of the producer: each after the first
     // once the producer has taken the previous one. It posts each with its
     // unit's entry, then -- for a w2 task -- waits (device scope) until the
     // unit's w13 tiles are all done and publishes that for the producer, so
     // the check runs while the producer still streams the previous task.
     if (lane == 0 && pre_ok) {
-      int task = static_cast<int>(blockIdx.x);
+      int task = first_task;
       uint32_t j = 0;
       bool ok = true;
-      if (pre) {  // task b is posted: claim the next once the producer has taken it
+      if (pre) {  // the first task is posted: claim the next once the producer has taken it
         j = 1;
         ok = wait_seq(&misc->prod_seq, 0, abort);
-        task = grid + atomicAdd(p.task_ctr, 1);
+        task = atomicAdd(p.task_ctr, 1);
       }
       for (; ok; ++j) {
         Task k = {0, 0, 0, 0, 0, 0};
         int4 a = make_int4(0, 0, 0, 0);
-        for (; task < ntasks; task = grid + atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
+        for (; task < ntasks; task = atomicAdd(p.task_ctr, 1)) {  // only valid tasks are posted
           k = decode_task(task, n13, w2full, p);
           const uint32_t v = unit_s[k.u];  // (expert id, first row, rows)
           a = make_int4(static_cast<int>(v & 1023u), static_cast<int>(v >> 16),
@@ -793,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         if (k.phase == 1 && !wait_ready(p.ready + k.u, p.t13, abort)) break;
         st_release_cta(&misc->ready_seq, static_cast<int>(j));
         if (!wait_seq(&misc->prod_seq, static_cast<int>(j), abort)) break;
-        task = grid + atomicAdd(p.task_ctr, 1);
+        task = atomicAdd(p.task_ctr, 1);
       }
     }
     __syncwarp();
@@ -821,6 +834,15 @@ cudaError_t expert_kernel_setup() {
     e = cudaFuncSetAttribute(expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes));
   return e;
+}
+
+cudaError_t expert_occupancy(int fp4, int* per_sm) {
+  cudaError_t e = expert_kernel_setup();
+  if (e != cudaSuccess) return e;
+  return fp4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, expert_kernel<true>, kThreads,
+                                                             kSmemBytes)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, expert_kernel<false>,
+                                                             kThreads, kSmemBytes);
 }
 
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s) {

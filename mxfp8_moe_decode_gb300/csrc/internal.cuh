@@ -93,6 +93,7 @@ struct RouterParams {
   int clear_n[3];
   float* zero_rows;  // floats all CTAs set to zero (the partial rows that w2 halves add into), or null
   size_t zero_n;
+  int* err;          // device error word: a bulk-copy wait that gives up sets kErrTimeout
   int M, H, E, KS, Hs;
 };
 
@@ -177,6 +178,8 @@ struct ExpertParams {
                               // tokens, g2 >= 4)
   int units_max;              // capacity of the active-expert table
   int rows_max;               // capacity of the partial-output rows
+  int withhold_unit;          // test hook: this unit's w13 tiles never report ready, so its
+                              // w2 tasks' bounded waits expire (-1: off)
   int M, K;                   // this step's tokens, picks per token
 };
 
@@ -247,6 +250,8 @@ size_t router_smem_bytes(int M, int Hs);
 int router_ksplit(int hidden, int experts);
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s);
 cudaError_t expert_kernel_setup();
+// CTAs of the expert kernel (routed format: fp4 = 1 for E2M1) one SM can hold
+cudaError_t expert_occupancy(int fp4, int* per_sm);
 size_t expert_smem_bytes(int phase);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_sfa_pack(const SfaPackParams& p, cudaStream_t s);

@@ -37,7 +37,10 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // First call on a device (that device current): find the array's device
-// address and raise the router kernel's shared-memory limit.
+// address and raise the router kernel's shared-memory limit. The address is
+// kept for the life of the process: a cudaDeviceReset, which unloads the
+// library's device code, makes it stale, so calls after a reset are not
+// supported.
 int device_scratch(int dev, void** addr) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
@@ -120,6 +123,7 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
     rp.clear[r] = nullptr;
     rp.clear_n[r] = 0;
   }
+  rp.err = reinterpret_cast<int*>(base + o_ctr) + kCtrErr;
   rp.zero_rows = nullptr;
   rp.zero_n = 0;
   rp.pf_bytes[0] = rp.pf_bytes[1] = 0;
@@ -151,5 +155,40 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
+  return MOE_OK;
+}
+
+extern "C" int moe_route_static_status(void* stream) {
+  using namespace moe;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CAPTURE;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return MOE_ERR_CAPTURE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    if (!g_ready[dev]) return MOE_OK;  // no call has run on this device
+    base = g_addr[dev];
+  }
+  // the error word is the first counter word of the array (see the layout in
+  // moe_route_static); read it behind the calls already enqueued on the stream
+  int word = 0;
+  if (cudaMemcpyAsync(&word, static_cast<int*>(base) + kCtrErr, 4, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (word & kErrBounds) return MOE_ERR_ARG;
   return MOE_OK;
 }

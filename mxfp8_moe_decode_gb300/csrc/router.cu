@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
   }
   __syncthreads();
 
+  bool landed = true;  // the K-slice of the normed rows is in shared memory
   if (p.x) {
     // ---- fused seam, in the seam's arithmetic and order (seam.cuh): first
     // every row's sum of squares -- thread t plays owner t & 127 for rows
@@ -220,7 +221,18 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
                        p.normed + static_cast<size_t>(m) * H + k0, Hs * 2, b);
     }
     int never = 0;
-    ptx::mbar_wait(ptx::smem_u32(&bar), 0, &never, kWaitLimitNs);
+    landed = ptx::mbar_wait(ptx::smem_u32(&bar), 0, &never, kWaitLimitNs);
+  }
+  // A bulk-copy wait that gave up: record it in the error word, let the
+  // copies still in flight land (bounded) so none writes into the shared
+  // memory of a later CTA, and skip the product and its stores.
+  if (!__syncthreads_and(landed)) {
+    if (tid == 0) {
+      if (p.err) atomicOr(p.err, kErrTimeout);
+      int never = 0;
+      ptx::mbar_wait(ptx::smem_u32(&bar), 0, &never, kWaitLimitNs);
+    }
+    return;
   }
   // ---- this CTA's share of the L2 prefetch (chunks b, b + ctas, ... of each
   // range), issued once the CTA's own loads have landed so that it does not

@@ -241,13 +241,15 @@ def test_small_m4():
         L.close()
 
 
-@pytest.mark.parametrize("name,sample", [("full_m1", None), ("full_m16", [0, 7, 15]),
-                                         ("full_m48_uniform", [0, 23, 47]),
-                                         ("full_m48_zipf", [0, 23, 47]),
+# every output row of every full-size workload against the oracle (which
+# evaluates each touched expert once over all the rows that picked it)
+@pytest.mark.parametrize("name,sample", [("full_m1", None), ("full_m16", None),
+                                         ("full_m48_uniform", None),
+                                         ("full_m48_zipf", None),
                                          ("full_e384_m1", None),
-                                         ("full_e384_m48", [0, 23, 47]),
+                                         ("full_e384_m48", None),
                                          ("full_e384_fp4_m1", None),
-                                         ("full_e384_fp4_m48", [0, 23, 47])])
+                                         ("full_e384_fp4_m48", None)])
 def test_full_size(name, sample):
     L = Layer(W.WORKLOADS[name])
     try:
