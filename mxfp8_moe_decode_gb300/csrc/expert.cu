@@ -28,7 +28,7 @@
 // readiness waits always end, however many of the grid's CTAs are resident
 // at once.
 //
-// Per CTA (one per SM, 288 threads):
+// Per CTA (one per SM, 352 threads):
 //  warp 8 lane 0, the scheduler, claims the CTA's tasks one ahead of the
 //    producer (the next one when the producer has kClaimLead stages of the
 //    current one left to issue, so that a w2 task is rarely claimed long
@@ -36,22 +36,23 @@
 //    in shared memory, and for a w2 task waits (device scope) for the unit's
 //    readiness and publishes it in shared memory. A device-scope wait in the
 //    producer thread would also wait for its copies in flight.
-//  warp 0 lane 0, the producer, issues the loads into an 8-stage ring -- per
+//  warp 0 lane 0, the producer, issues the loads into an 8-slot ring -- per
 //    stage one weight box (TMA, evict-first from L2) and one contiguous bulk
 //    copy of the activation panel (rows + scale image, already in the
-//    swizzled layout the MMA reads, evict-last).
+//    swizzled layout the MMA reads, evict-last). Each slot belongs to one
+//    MMA issuer (two slots each), which waits for every phase of it.
 //  warp 3 writes each stage's weight-scale image (the stage's 16-byte entry in
 //    all 32 rows tcgen05.cp expects) as soon as the slot is free.
-//  lane 0 of warps 1 and 2, the MMA issuers, share the stages of every task:
-//    warp 1 takes the even K stages, warp 2 (which also owns the TMEM
-//    allocation) the odd ones; each copies its stage's two scale images into
-//    TMEM and issues 4 MMAs (K = 32 each, the descriptor's scale-factor id
-//    picks the K block of the stage) into its own accumulator, and the
-//    epilogue adds the two partial sums. One thread needs ~530 cycles to
-//    issue a stage (about 100 per MMA, 55 per scale copy); that is more than
-//    the ~720 cycles per 16 KB stage at which one SM's share of HBM arrives,
-//    minus the slot's other costs, while two issuers work concurrently at the
-//    same per-thread rate.
+//  lane 0 of warps 1, 2, 9 and 10, the MMA issuers, share the stages of
+//    every task: issuer h (warp 1, 2 -- which also owns the TMEM allocation
+//    -- 9, 10) takes the K stages g with g mod 4 = h; each copies its stage's
+//    two scale images into TMEM and issues 4 MMAs (K = 32 each, the
+//    descriptor's scale-factor id picks the K block of the stage) into its
+//    own accumulator, and the epilogue adds the partial sums in issuer order.
+//    One thread needs ~530 cycles to issue a stage (about 100 per MMA, 55 per
+//    scale copy), near the ~720 cycles per 16 KB stage at which one SM's
+//    share of HBM arrives, and an MXFP4 stage carries half those bytes; the
+//    issuers work concurrently at the same per-thread rate.
 //  warps 4-7 drain the double-buffered accumulators (each reads its 32-lane
 //    quarter).
 //
@@ -63,8 +64,8 @@
 // and descriptors as with E4M3 and only the instruction descriptor's A
 // format changes. The per-row codes differ across all 128 rows of a tile, so
 // each stage's scale image (lane i, cell c = row 32 c + i) is prepacked at
-// creation and copied by the producer with the weights (the image warp only
-// marks those slots ready). The shared expert stays E4M3.
+// creation and copied into the slot by the image warp. The shared expert
+// stays E4M3.
 // Every mbarrier and readiness wait is bounded; on a timeout the CTA records
 // kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
 //
@@ -79,7 +80,7 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 288;  // 9 warps
+constexpr int kThreads = 352;  // 11 warps
 constexpr uint32_t kABytes = kTileM * kStageK;           // 16 KB
 constexpr uint32_t kImgBytes = 32 * 16;                  // scale image of one stage
 constexpr uint32_t kBBytes = 7 * 1024;  // one activation panel (<= 48 rows + image), 1024-aligned
@@ -92,10 +93,25 @@ constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kOffUnits = kOffMisc + 512;                     // packed unit entries
 constexpr uint32_t kSmemUsed = kOffUnits + ((kMaxExperts + 1) * 4 + 15) / 16 * 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
-// TMEM: 2 task buffers x 2 issuers x 64 accumulator columns, then 8 scale columns per stage
+// MMA issuer threads per CTA: stage g of a task goes to issuer g mod kIssuers,
+// each into its own accumulator, and the epilogue adds them in issuer order
+// (a split that depends on g alone, so the sums are the same in every run).
+// The ring's slots are owned by the issuers -- issuer h uses slots h and
+// h + kIssuers in turn -- so every waiter on a slot's barriers sees each of
+// its phases: with slots shared round-robin among several consumers, a
+// consumer could test a slot whose previous phase it never waited for and
+// take that phase's parity for the one it wants.
+constexpr int kIssuers = 4;
+static_assert(kStages == 2 * kIssuers, "two ring slots per issuer");
+// TMEM: 2 task buffers x kIssuers issuers x 64 accumulator columns; an
+// accumulator uses at most kMaxTokens columns, and ring slot s keeps its 8
+// scale columns (4 for the weights, 4 for the activations) in the unused
+// tail of the s-th 64-column block
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 64;
-constexpr uint32_t kSfCol0 = 4 * kAccCols;
+constexpr uint32_t kSfColOff = kMaxTokens;
+static_assert(2 * kIssuers * kAccCols == kTmemCols, "TMEM budget");
+static_assert(kSfColOff + 8 <= kAccCols, "scale columns beside the accumulator columns");
 constexpr int kTaskSlots = 8;  // task-id queue from the scheduler warp to the other roles
 // The producer lets the scheduler claim the next task when this many of the
 // current task's stages are left to issue (the ring holds 8 more): late enough
@@ -106,7 +122,6 @@ constexpr int kClaimLead = 10;
 static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "B tiles must stay 1024-aligned");
 static_assert(kBBytes >= kPanelPitch, "a panel fits its slot");
 static_assert(kOffSfa % 512 == 0, "scale images alignment");
-static_assert(kSfCol0 + kStages * 8 <= kTmemCols, "TMEM budget");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Bars {
@@ -117,7 +132,7 @@ struct Bars {
   uint64_t tempty[2];
   uint64_t drain;
   uint64_t task_full[kTaskSlots];   // the producer posted a task id
-  uint64_t task_empty[kTaskSlots];  // its five readers (kTaskReaders) have taken it
+  uint64_t task_empty[kTaskSlots];  // its readers (kTaskReaders) have taken it
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
 
@@ -224,7 +239,7 @@ __device__ __forceinline__ bool wait_ready(const int* ctr, int target, volatile 
 // The j-th task of this CTA: the scheduler posts its id (-1: no more tasks)
 // with its unit's table entry; each of the five readers takes both and frees
 // the slot at once. A reader gets -2 when a wait gave up (the abort flag is set).
-constexpr int kTaskReaders = 5;  // producer, two MMA issuers, scale-image warp, epilogue
+constexpr int kTaskReaders = 3 + kIssuers;  // producer, MMA issuers, scale-image warp, epilogue
 // A decoded task in 16 bytes: phase, half and tile; unit; first stage and
 // stage count.
 __device__ __forceinline__ int4 pack_task(const Task& k) {
@@ -308,6 +323,28 @@ __device__ __forceinline__ bool wait_seq(const int* seq, int j, volatile int* ab
   }
 }
 
+// Ring slots of the stages as a role that walks every stage in order sees
+// them: stage g of a task belongs to issuer h = g mod kIssuers, whose stages
+// take slots h and h + kIssuers in turn; per slot, the parity of the phase to
+// wait for next (its earlier uses, mod 2) and whether it was used at all.
+struct SlotWalk {
+  uint32_t next = 0;     // bit h: issuer h's next stage takes slot h + kIssuers
+  uint32_t par = 0;      // bit s: slot s's uses so far, mod 2
+  uint32_t touched = 0;  // bit s: slot s used at least once
+  __device__ __forceinline__ int slot(int g) const {
+    const int h = g % kIssuers;
+    return h + kIssuers * static_cast<int>((next >> h) & 1u);
+  }
+  __device__ __forceinline__ uint32_t parity(int s) const { return (par >> s) & 1u; }
+  __device__ __forceinline__ void advance(int g, int s) {
+    next ^= 1u << (g % kIssuers);
+    par ^= 1u << s;
+    touched |= 1u << s;
+  }
+  // parity of the last phase armed on slot s (touched slots only)
+  __device__ __forceinline__ uint32_t last_parity(int s) const { return parity(s) ^ 1u; }
+};
+
 // kFp4: the routed experts are MXFP4 (E2M1 with per-row scale images); the
 // E4M3 instantiation carries none of that path's code.
 template <bool kFp4>
@@ -327,10 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       ptx::mbar_init(ptx::smem_u32(&bars->sfa_rdy[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(ptx::smem_u32(&bars->tfull[a]), 2);   // one commit per issuer
+      ptx::mbar_init(ptx::smem_u32(&bars->tfull[a]), kIssuers);  // one commit per issuer
       ptx::mbar_init(ptx::smem_u32(&bars->tempty[a]), 4);  // one arrival per epilogue warp
     }
-    ptx::mbar_init(ptx::smem_u32(&bars->drain), 2);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), kIssuers);
     for (int q = 0; q < kTaskSlots; ++q) {
       ptx::mbar_init(ptx::smem_u32(&bars->task_full[q]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->task_empty[q]), kTaskReaders);
@@ -361,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
-      uint32_t it = 0;
+      SlotWalk walk;
       bool ok = true;
       // Weight stages are issued at once. A w2 task's activation stages are
       // held back (at most one ring's worth) until its unit's w13 tiles are
@@ -376,16 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         const int nt = (a.z + 15) & ~15;
         const uint32_t pbytes = kPanelRows + nt * 128;  // the panel's used part
         const bool shared_e = a.x == p.E;
-        // MXFP4 routed weights: the stage's per-row scale image comes with
-        // the weights (one 512-byte copy) instead of from the image warp; a
-        // 4-bit weight box counts its global bytes (two codes per byte), half
-        // of what it fills in shared memory
-        const bool img = kFp4 && !shared_e;
-        const uint32_t bytes = (img ? kABytes / 2 + kImgBytes : kABytes) + pbytes;
-        const uint4* img_src =
-            !img ? nullptr
-                 : (k.phase ? p.img2 + ((static_cast<size_t>(a.x) * p.t2 + k.t) * p.g2 + k.g0) * 32
-                            : p.img13 + ((static_cast<size_t>(a.x) * p.t13 + k.t) * p.g13 + k.g0) * 32);
+        // MXFP4 routed weights: a 4-bit weight box counts its global bytes
+        // (two codes per byte), half of what it fills in shared memory
+        const bool fp4 = kFp4 && !shared_e;
+        const uint32_t bytes = (fp4 ? kABytes / 2 : kABytes) + pbytes;
         const int G = k.gn;
         const int panels = k.phase ? p.g2 : p.g13;  // per unit (h) or expert (x)
         // x panels are kept per expert id (a lone token's experts all read
@@ -400,21 +431,23 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
                          ptx::smem_u32(&bars->full[s]), pol_x);
         };
         bool b_ok = k.phase == 0;
-        int first_pending = 0, n_pending = 0;
+        int pend_g0 = 0, n_pending = 0;
+        uint32_t pend_s = 0;  // slots of the held-back stages pend_g0, pend_g0 + 1, ... (4 bits each)
+        static_assert(kStages <= 8, "held-back slots packed in 32 bits");
         const int claim_g = G > kClaimLead ? G - kClaimLead : 0;
-        for (int g = 0; g < G; ++g, ++it) {
+        for (int g = 0; g < G; ++g) {
           if (g == claim_g) st_release_cta(&misc->prod_seq, static_cast<int>(j));  // claim the next
-          const int s = it % kStages;
-          const uint32_t round = it / kStages;
-          if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty[s]), (round & 1) ^ 1, abort,
+          const int s = walk.slot(g);
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty[s]), walk.parity(s) ^ 1u, abort,
                               kWaitLimitNs)) {
             // the held-back activation copies of the stages already expected
             // still go out, so that each of those stages completes before exit
             for (int q = 0; q < n_pending; ++q)
-              issue_b(g - n_pending + q, static_cast<int>((first_pending + q) % kStages));
+              issue_b(pend_g0 + q, static_cast<int>((pend_s >> (4 * q)) & 15u));
             ok = false;
             break;
           }
+          walk.advance(g, s);
           const uint32_t full = ptx::smem_u32(&bars->full[s]);
           ptx::mbar_arrive_expect_tx(full, bytes);
           const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
@@ -427,14 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
             ptx::tma_load_2d(sa, shared_e ? &p.tm_w2_shared : &p.tm_w2, x,
                              (shared_e ? 0 : a.x * p.hidden) + kTileM * k.t, full, pol_w);
           }
-          if (img)
-            ptx::bulk_load(ptx::smem_u32(smem + kOffSfa + s * kImgBytes), img_src + g * 32,
-                           kImgBytes, full, pol_w);
           if (b_ok) {
             issue_b(g, s);
           } else {
-            if (n_pending == 0) first_pending = it;
-            ++n_pending;
+            if (n_pending == 0) {
+              pend_g0 = g;
+              pend_s = 0;
+            }
+            pend_s |= static_cast<uint32_t>(s) << (4 * n_pending++);
             bool go = k.phase == 1 && ld_acquire_cta(&misc->ready_seq) >= static_cast<int>(j);
             if (!go && (n_pending == kStages || g == G - 1)) {
               // on a timeout the held-back loads still go out (their data is
@@ -445,34 +478,26 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
             if (go) {
               if (k.phase == 1) asm volatile("fence.proxy.async.global;" ::: "memory");
               b_ok = true;
-              const int g0 = g - (n_pending - 1);
               for (int q = 0; q < n_pending; ++q)
-                issue_b(g0 + q, static_cast<int>((first_pending + q) % kStages));
+                issue_b(pend_g0 + q, static_cast<int>((pend_s >> (4 * q)) & 15u));
               n_pending = 0;
-              if (!ok) {
-                ++it;  // count this stage for the drain below
-                break;
-              }
+              if (!ok) break;
             }
           }
         }
       }
       // wait for every copy still in flight before the CTA may exit
-      const uint32_t issued = it;
-      for (int s = 0; s < kStages; ++s) {
-        if (static_cast<uint32_t>(s) < issued) {
-          const uint32_t last_round = (issued - 1 - s) / kStages;
-          drain_wait(ptx::smem_u32(&bars->full[s]), last_round & 1);
-        }
-      }
+      for (int s = 0; s < kStages; ++s)
+        if ((walk.touched >> s) & 1u) drain_wait(ptx::smem_u32(&bars->full[s]), walk.last_parity(s));
     }
     __syncwarp();
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp == 1 || warp == 2 || warp == 9 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers
-    // issuer h takes the stages g with g % 2 == h of every task
-    const int h = warp - 1;
+    // issuer h takes the stages g with g % kIssuers == h of every task; its
+    // n-th stage overall sits in its ring slot h + kIssuers (n % 2)
+    const int h = warp >= 9 ? warp - 7 : warp - 1;
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t n_own = 0;
       int lt = 0;
       bool ok = true;
       for (uint32_t j = 0; ok; ++j) {
@@ -482,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         if (task < 0) break;
         const int nt = (a.z + 15) & ~15;
         const uint32_t a_fmt = (kFp4 && a.x != p.E) ? ptx::kFmtE2M1 : ptx::kFmtE4M3;
-        const int G = k.gn;  // at least 2: both issuers write their accumulator
+        const int G = k.gn;  // >= 2; an issuer with no stage leaves its accumulator unused
         const int acc = lt & 1;
         const uint32_t use = static_cast<uint32_t>(lt) >> 1;
         ++lt;
@@ -491,18 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tbase + (2 * acc + h) * kAccCols;
-        for (int g = 0; g < G; ++g, ++it) {
-          if ((g & 1) != h) continue;
-          const int s = it % kStages;
-          const uint32_t round = it / kStages;
-          if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[s]), round & 1, abort, kWaitLimitNs) ||
-              !ptx::mbar_wait(ptx::smem_u32(&bars->sfa_rdy[s]), round & 1, abort, kWaitLimitNs)) {
+        const uint32_t d_tmem = tbase + (kIssuers * acc + h) * kAccCols;
+        for (int g = h; g < G; g += kIssuers, ++n_own) {
+          const int s = h + kIssuers * static_cast<int>(n_own & 1u);
+          const uint32_t parity = (n_own >> 1) & 1u;  // the slot's earlier uses, mod 2
+          if (!ptx::mbar_wait(ptx::smem_u32(&bars->full[s]), parity, abort, kWaitLimitNs) ||
+              !ptx::mbar_wait(ptx::smem_u32(&bars->sfa_rdy[s]), parity, abort, kWaitLimitNs)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sf_a = tbase + kSfCol0 + s * 8;
+          const uint32_t sf_a = tbase + s * kAccCols + kSfColOff;
           const uint32_t sf_b = sf_a + 4;
           const uint32_t sa = ptx::smem_u32(smem + kOffA + s * kABytes);
           const uint32_t sp = ptx::smem_u32(smem + kOffB + s * kBBytes);  // scale image, then rows
@@ -513,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
           for (int kk = 0; kk < 4; ++kk) {
             ptx::tc_mma_mxf8(d_tmem, ptx::sdesc_k128_sw128(sa + 32 * kk),
                              ptx::sdesc_k128_sw128(sb + 32 * kk), ptx::idesc_mxf8(nt, kk, a_fmt), sf_a,
-                             sf_b, (g > h) || kk != 0);
+                             sf_b, (g >= kIssuers) || kk != 0);
           }
           ptx::tc_commit(ptx::smem_u32(&bars->empty[s]));
         }
@@ -527,10 +551,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ weight-scale images
-    // Runs ahead of the MMA issuer: as soon as a ring slot is free it writes the
-    // slot's 32 x 16-byte image (the stage's 16-byte entry in every row).
-    uint32_t it = 0;
+    // Runs ahead of the MMA issuers: as soon as a ring slot is free it writes
+    // the slot's 32 x 16-byte image (the stage's 16-byte entry in every row);
+    // for MXFP4 routed weights it copies the stage's prepacked per-row image
+    // (512 bytes, completing on the slot's sfa_rdy barrier) instead, which
+    // keeps that copy off the producer thread.
+    SlotWalk walk;
     bool ok = true;
+    const uint64_t pol_img = ptx::policy_evict_first();
     for (uint32_t j = 0; ok; ++j) {
       int4 a = make_int4(0, 0, 0, 0);
       Task k0 = {0, 0, 0, 0, 0, 0};
@@ -546,23 +574,32 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       k.gn = __shfl_sync(0xffffffffu, k0.gn, 0);
       k.half = __shfl_sync(0xffffffffu, k0.half, 0);
       const int G = k.gn;
-      // MXFP4 routed weights: the producer copies the stage's image itself
+      // MXFP4 routed weights: the stage's image is copied from the prepacked ones
       const bool copied = kFp4 && ex != p.E;
+      const uint4* img_src =
+          !copied ? nullptr
+                  : (k.phase ? p.img2 + ((static_cast<size_t>(ex) * p.t2 + k.t) * p.g2 + k.g0) * 32
+                             : p.img13 + ((static_cast<size_t>(ex) * p.t13 + k.t) * p.g13 + k.g0) * 32);
       const uint4* sfa = (k.phase ? p.sfa2 + (static_cast<size_t>(ex) * p.t2 + k.t) * p.g2
                                   : p.sfa13 + (static_cast<size_t>(ex) * p.t13 + k.t) * p.g13) +
                          k.g0;
       const uint4 zero = make_uint4(0, 0, 0, 0);
       const uint4 e0 = !copied && lane < G ? __ldg(sfa + lane) : zero;  // stages lane, lane + 32
       const uint4 e1 = !copied && lane + 32 < G ? __ldg(sfa + lane + 32) : zero;
-      for (int g = 0; g < G; ++g, ++it) {
-        const int s = it % kStages;
-        const uint32_t round = it / kStages;
-        if (!warp_wait(ptx::smem_u32(&bars->empty[s]), (round & 1) ^ 1, abort)) {
+      for (int g = 0; g < G; ++g) {
+        const int s = walk.slot(g);
+        if (!warp_wait(ptx::smem_u32(&bars->empty[s]), walk.parity(s) ^ 1u, abort)) {
           ok = false;
           break;
         }
+        walk.advance(g, s);
         if (copied) {
-          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->sfa_rdy[s]));
+          if (lane == 0) {
+            const uint32_t rdy = ptx::smem_u32(&bars->sfa_rdy[s]);
+            ptx::mbar_arrive_expect_tx(rdy, kImgBytes);
+            ptx::bulk_load(ptx::smem_u32(smem + kOffSfa + s * kImgBytes), img_src + g * 32,
+                           kImgBytes, rdy, pol_img);
+          }
           continue;
         }
         const uint4 src = g < 32 ? e0 : e1;
@@ -577,6 +614,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->sfa_rdy[s]));
       }
     }
+    // image copies still in flight land before the CTA may exit
+    if (kFp4 && lane == 0) {
+      for (int s = 0; s < kStages; ++s)
+        if ((walk.touched >> s) & 1u)
+          drain_wait(ptx::smem_u32(&bars->sfa_rdy[s]), walk.last_parity(s));
+    }
+    __syncwarp();
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp - 4;  // TMEM lane quarter
@@ -607,20 +651,27 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       ptx::mbar_wait(tfull, use & 1, abort, kWaitLimitNs);  // completed: returns at once
       ptx::tc_fence_after();
       float v[kMaxTokens];
-      // the even-stage issuer's sums, then the odd-stage issuer's added 16
-      // columns at a time (one 16-register buffer)
-      const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * q) << 16) + 2 * acc * kAccCols;
+      // issuer 0's sums, then each later issuer's added in issuer order, 16
+      // columns at a time (one 16-register buffer); an issuer that had no
+      // stage in this task (fewer stages than issuers) is skipped
+      const uint32_t taddr =
+          tbase + (static_cast<uint32_t>(32 * q) << 16) + kIssuers * acc * kAccCols;
       ptx::tmem_ld_32x32b_x16(taddr, v);
       if (nt > 16) ptx::tmem_ld_32x32b_x16(taddr + 16, v + 16);
       if (nt > 32) ptx::tmem_ld_32x32b_x16(taddr + 32, v + 32);
+      ptx::tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < kMaxTokens / 16; ++c) {
-        if (16 * c < nt) {
-          float w[16];
-          ptx::tmem_ld_32x32b_x16(taddr + kAccCols + 16 * c, w);
-          ptx::tmem_wait_ld();
+      for (int h = 1; h < kIssuers; ++h) {
+        if (h >= k.gn) break;
 #pragma unroll
-          for (int n = 0; n < 16; ++n) v[16 * c + n] += w[n];
+        for (int c = 0; c < kMaxTokens / 16; ++c) {
+          if (16 * c < nt) {
+            float w[16];
+            ptx::tmem_ld_32x32b_x16(taddr + h * kAccCols + 16 * c, w);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int n = 0; n < 16; ++n) v[16 * c + n] += w[n];
+          }
         }
       }
       ptx::tc_fence_before();
