@@ -153,8 +153,9 @@ typedef struct moe_handle moe_handle;
  * MOE_ROUTED_E2M1 the routed w13 / w2 not 32-byte aligned), MOE_ERR_DEVICE,
  * MOE_ERR_CUDA, MOE_ERR_CAPTURE (the legacy stream of `device` is being
  * captured: creation allocates and synchronises), and MOE_ERR_UNSUPPORTED
- * also when one CTA of the expert kernel (352 threads, about 216 KB of shared
- * memory) cannot be resident on an SM of this device. With MOE_ROUTED_E2M1 the
+ * also when one CTA of the expert kernel (384 threads, 448 with
+ * MOE_ROUTED_E2M1; about 216 KB of shared memory) cannot be resident on an SM
+ * of this device. With MOE_ROUTED_E2M1 the
  * handle also holds the routed experts' per-row scale codes regrouped for the
  * tensor cores (as many bytes as w13_s and w2_s).
  *

@@ -260,7 +260,8 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MOE_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_DEVICE;
   if (!get_encode_fn()) return MOE_ERR_CUDA;
-  // one expert CTA (352 threads, ~216 KB of shared memory) must fit an SM
+  // one expert CTA (384 threads, 448 with MXFP4 routed experts; ~216 KB of shared
+  // memory) must fit an SM
   {
     int per_sm = 0;
     const cudaError_t e =

@@ -28,7 +28,7 @@
 // readiness waits always end, however many of the grid's CTAs are resident
 // at once.
 //
-// Per CTA (one per SM, 352 threads):
+// Per CTA (one per SM, 384 threads; 448 with MXFP4 routed experts):
 //  warp 8 lane 0, the scheduler, claims the CTA's tasks one ahead of the
 //    producer (the next one when the producer has kClaimLead stages of the
 //    current one left to issue, so that a w2 task is rarely claimed long
@@ -36,11 +36,15 @@
 //    in shared memory, and for a w2 task waits (device scope) for the unit's
 //    readiness and publishes it in shared memory. A device-scope wait in the
 //    producer thread would also wait for its copies in flight.
-//  warp 0 lane 0, the producer, issues the loads into an 8-slot ring -- per
+//  lane 0 of warp 0 and warps 11 ..., the producers (two with E4M3 routed
+//    experts, four with MXFP4), issue the loads into an 8-slot ring -- per
 //    stage one weight box (TMA, evict-first from L2) and one contiguous bulk
 //    copy of the activation panel (rows + scale image, already in the
-//    swizzled layout the MMA reads, evict-last). Each slot belongs to one
-//    MMA issuer (two slots each), which waits for every phase of it.
+//    swizzled layout the MMA reads, evict-last). Each slot belongs to one MMA
+//    issuer (two slots each), which waits for every phase of it, and each
+//    producer fills the slots of its issuers: a thread issuing TMA copies
+//    spends a fixed time per copy, so several producers keep the ring full at
+//    HBM speed.
 //  warp 3 writes each stage's weight-scale image (the stage's 16-byte entry in
 //    all 32 rows tcgen05.cp expects) as soon as the slot is free.
 //  lane 0 of warps 1, 2, 9 and 10, the MMA issuers, share the stages of
@@ -64,8 +68,8 @@
 // and descriptors as with E4M3 and only the instruction descriptor's A
 // format changes. The per-row codes differ across all 128 rows of a tile, so
 // each stage's scale image (lane i, cell c = row 32 c + i) is prepacked at
-// creation and copied into the slot by the image warp. The shared expert
-// stays E4M3.
+// creation and copied into the slot by the producer with the weights (the
+// image warp only marks those slots ready). The shared expert stays E4M3.
 // Every mbarrier and readiness wait is bounded; on a timeout the CTA records
 // kErrTimeout, waits for its own copies and MMAs, frees TMEM and exits.
 //
@@ -80,7 +84,6 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 352;  // 11 warps
 constexpr uint32_t kABytes = kTileM * kStageK;           // 16 KB
 constexpr uint32_t kImgBytes = 32 * 16;                  // scale image of one stage
 constexpr uint32_t kBBytes = 7 * 1024;  // one activation panel (<= 48 rows + image), 1024-aligned
@@ -103,6 +106,22 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the bas
 // take that phase's parity for the one it wants.
 constexpr int kIssuers = 4;
 static_assert(kStages == 2 * kIssuers, "two ring slots per issuer");
+// TMA-issuing threads (producers): a thread that issues the ring's copies
+// spends a fixed ~400 ns per tensor box and ~45 ns per small bulk copy
+// (measured on a bare ring, whatever the box's bytes), which caps one thread
+// near 3 TB/s over the GPU for the 8 KB boxes of MXFP4 weights. Measured
+// there: an E4M3 stage (box + activation panel) reaches HBM speed with two
+// producers, an MXFP4 stage (box + scale image + panel) only with four. Each
+// producer feeds the slots of kIssuers / producers issuers. Warps: 0 the first
+// producer, 1, 2, 9, 10 the issuers, 3 the scale images, 4-7 the epilogue,
+// 8 the scheduler, 11 ... the other producers.
+template <bool kFp4>
+struct Roles {
+  static constexpr int kProducers = kFp4 ? 4 : 2;
+  static constexpr int kThreads = (10 + kProducers) * 32;
+  static constexpr int kTaskReaders = 2 + kProducers + kIssuers;  // producers, issuers, images, epilogue
+  static_assert(kIssuers % kProducers == 0, "issuers split evenly among the producers");
+};
 // TMEM: 2 task buffers x kIssuers issuers x 64 accumulator columns; an
 // accumulator uses at most kMaxTokens columns, and ring slot s keeps its 8
 // scale columns (4 for the weights, 4 for the activations) in the unused
@@ -239,7 +258,6 @@ __device__ __forceinline__ bool wait_ready(const int* ctr, int target, volatile 
 // The j-th task of this CTA: the scheduler posts its id (-1: no more tasks)
 // with its unit's table entry; each of the five readers takes both and frees
 // the slot at once. A reader gets -2 when a wait gave up (the abort flag is set).
-constexpr int kTaskReaders = 3 + kIssuers;  // producer, MMA issuers, scale-image warp, epilogue
 // A decoded task in 16 bytes: phase, half and tile; unit; first stage and
 // stage count.
 __device__ __forceinline__ int4 pack_task(const Task& k) {
@@ -348,7 +366,9 @@ struct SlotWalk {
 // kFp4: the routed experts are MXFP4 (E2M1 with per-row scale images); the
 // E4M3 instantiation carries none of that path's code.
 template <bool kFp4>
-__global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_constant__ ExpertParams p) {
+__global__ void __launch_bounds__(Roles<kFp4>::kThreads, 1)
+    expert_kernel(const __grid_constant__ ExpertParams p) {
+  constexpr int kProducers = Roles<kFp4>::kProducers;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -370,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     ptx::mbar_init(ptx::smem_u32(&bars->drain), kIssuers);
     for (int q = 0; q < kTaskSlots; ++q) {
       ptx::mbar_init(ptx::smem_u32(&bars->task_full[q]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->task_empty[q]), kTaskReaders);
+      ptx::mbar_init(ptx::smem_u32(&bars->task_empty[q]), Roles<kFp4>::kTaskReaders);
     }
     misc->abort = 0;
     misc->epi_ok = 0;
@@ -393,8 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
   const uint32_t tbase = misc->tmem_base;
 
   uint32_t* unit_s = reinterpret_cast<uint32_t*>(smem + kOffUnits);
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp >= 11) {
+    // ------------------------------------------------------------ TMA producers
+    // producer q (warp 0: q = 0, warps 11 ...: q = 1 ...) issues the stages g
+    // with g mod kIssuers in [q kIssuers / kProducers, (q + 1) kIssuers /
+    // kProducers), i.e. the stages of its issuers, in increasing g
+    const int q = warp == 0 ? 0 : warp - 10;
+    constexpr int kPerProducer = kIssuers / kProducers;
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
@@ -416,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         // MXFP4 routed weights: a 4-bit weight box counts its global bytes
         // (two codes per byte), half of what it fills in shared memory
         const bool fp4 = kFp4 && !shared_e;
-        const uint32_t bytes = (fp4 ? kABytes / 2 : kABytes) + pbytes;
+        const uint32_t bytes = (fp4 ? kABytes / 2 + kImgBytes : kABytes) + pbytes;
         const int G = k.gn;
         const int panels = k.phase ? p.g2 : p.g13;  // per unit (h) or expert (x)
         // x panels are kept per expert id (a lone token's experts all read
@@ -431,19 +456,36 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
                          ptx::smem_u32(&bars->full[s]), pol_x);
         };
         bool b_ok = k.phase == 0;
-        int pend_g0 = 0, n_pending = 0;
-        uint32_t pend_s = 0;  // slots of the held-back stages pend_g0, pend_g0 + 1, ... (4 bits each)
-        static_assert(kStages <= 8, "held-back slots packed in 32 bits");
+        int n_pending = 0;
+        uint64_t pend = 0;  // held-back stages: (g << 4 | slot) in 16 bits each
+        static_assert(kStages / kProducers <= 4 && kStages <= 16, "held-back stages in 64 bits");
+        // MXFP4 routed weights: the stage's prepacked per-row scale image
+        // (512 bytes) comes with the stage, under the same barrier
+        const uint4* img_src =
+            !fp4 ? nullptr
+                 : (k.phase ? p.img2 + ((static_cast<size_t>(a.x) * p.t2 + k.t) * p.g2 + k.g0) * 32
+                            : p.img13 + ((static_cast<size_t>(a.x) * p.t13 + k.t) * p.g13 + k.g0) * 32);
         const int claim_g = G > kClaimLead ? G - kClaimLead : 0;
+        bool claimed = q != 0;  // producer 0 lets the scheduler claim the next task
+        // the last stage of this producer's issuers in the task
+        int g_last = -1;
+        for (int g = G - 1; g >= 0 && g_last < 0; --g)
+          if ((g % kIssuers) / kPerProducer == q) g_last = g;
         for (int g = 0; g < G; ++g) {
-          if (g == claim_g) st_release_cta(&misc->prod_seq, static_cast<int>(j));  // claim the next
+          if (!claimed && g >= claim_g) {
+            st_release_cta(&misc->prod_seq, static_cast<int>(j));  // claim the next
+            claimed = true;
+          }
+          if ((g % kIssuers) / kPerProducer != q) continue;
           const int s = walk.slot(g);
           if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty[s]), walk.parity(s) ^ 1u, abort,
                               kWaitLimitNs)) {
             // the held-back activation copies of the stages already expected
             // still go out, so that each of those stages completes before exit
-            for (int q = 0; q < n_pending; ++q)
-              issue_b(pend_g0 + q, static_cast<int>((pend_s >> (4 * q)) & 15u));
+            for (int i = 0; i < n_pending; ++i) {
+              const uint32_t e = static_cast<uint32_t>(pend >> (16 * i));
+              issue_b(static_cast<int>((e >> 4) & 0xfffu), static_cast<int>(e & 15u));
+            }
             ok = false;
             break;
           }
@@ -460,16 +502,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
             ptx::tma_load_2d(sa, shared_e ? &p.tm_w2_shared : &p.tm_w2, x,
                              (shared_e ? 0 : a.x * p.hidden) + kTileM * k.t, full, pol_w);
           }
+          if (fp4)
+            ptx::bulk_load(ptx::smem_u32(smem + kOffSfa + s * kImgBytes), img_src + g * 32,
+                           kImgBytes, full, pol_w);
           if (b_ok) {
             issue_b(g, s);
           } else {
-            if (n_pending == 0) {
-              pend_g0 = g;
-              pend_s = 0;
-            }
-            pend_s |= static_cast<uint32_t>(s) << (4 * n_pending++);
+            if (n_pending == 0) pend = 0;
+            pend |= static_cast<uint64_t>((static_cast<uint32_t>(g) << 4) | static_cast<uint32_t>(s))
+                    << (16 * n_pending++);
             bool go = k.phase == 1 && ld_acquire_cta(&misc->ready_seq) >= static_cast<int>(j);
-            if (!go && (n_pending == kStages || g == G - 1)) {
+            if (!go && (n_pending == kStages / kProducers || g == g_last)) {
               // on a timeout the held-back loads still go out (their data is
               // not used), so that every issued stage completes before exit
               if (k.phase == 1 && !wait_seq(&misc->ready_seq, static_cast<int>(j), abort)) ok = false;
@@ -478,13 +521,16 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
             if (go) {
               if (k.phase == 1) asm volatile("fence.proxy.async.global;" ::: "memory");
               b_ok = true;
-              for (int q = 0; q < n_pending; ++q)
-                issue_b(pend_g0 + q, static_cast<int>((pend_s >> (4 * q)) & 15u));
+              for (int i = 0; i < n_pending; ++i) {
+                const uint32_t e = static_cast<uint32_t>(pend >> (16 * i));
+                issue_b(static_cast<int>((e >> 4) & 0xfffu), static_cast<int>(e & 15u));
+              }
               n_pending = 0;
               if (!ok) break;
             }
           }
         }
+        if (!claimed) st_release_cta(&misc->prod_seq, static_cast<int>(j));
       }
       // wait for every copy still in flight before the CTA may exit
       for (int s = 0; s < kStages; ++s)
@@ -553,12 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
     // ------------------------------------------------------------ weight-scale images
     // Runs ahead of the MMA issuers: as soon as a ring slot is free it writes
     // the slot's 32 x 16-byte image (the stage's 16-byte entry in every row);
-    // for MXFP4 routed weights it copies the stage's prepacked per-row image
-    // (512 bytes, completing on the slot's sfa_rdy barrier) instead, which
-    // keeps that copy off the producer thread.
+    // for MXFP4 routed weights the producer copies the stage's prepacked
+    // per-row image with the weights and this warp only marks the slot ready.
     SlotWalk walk;
     bool ok = true;
-    const uint64_t pol_img = ptx::policy_evict_first();
     for (uint32_t j = 0; ok; ++j) {
       int4 a = make_int4(0, 0, 0, 0);
       Task k0 = {0, 0, 0, 0, 0, 0};
@@ -574,12 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
       k.gn = __shfl_sync(0xffffffffu, k0.gn, 0);
       k.half = __shfl_sync(0xffffffffu, k0.half, 0);
       const int G = k.gn;
-      // MXFP4 routed weights: the stage's image is copied from the prepacked ones
+      // MXFP4 routed weights: the producer copies the stage's image itself
       const bool copied = kFp4 && ex != p.E;
-      const uint4* img_src =
-          !copied ? nullptr
-                  : (k.phase ? p.img2 + ((static_cast<size_t>(ex) * p.t2 + k.t) * p.g2 + k.g0) * 32
-                             : p.img13 + ((static_cast<size_t>(ex) * p.t13 + k.t) * p.g13 + k.g0) * 32);
       const uint4* sfa = (k.phase ? p.sfa2 + (static_cast<size_t>(ex) * p.t2 + k.t) * p.g2
                                   : p.sfa13 + (static_cast<size_t>(ex) * p.t13 + k.t) * p.g13) +
                          k.g0;
@@ -594,12 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         }
         walk.advance(g, s);
         if (copied) {
-          if (lane == 0) {
-            const uint32_t rdy = ptx::smem_u32(&bars->sfa_rdy[s]);
-            ptx::mbar_arrive_expect_tx(rdy, kImgBytes);
-            ptx::bulk_load(ptx::smem_u32(smem + kOffSfa + s * kImgBytes), img_src + g * 32,
-                           kImgBytes, rdy, pol_img);
-          }
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->sfa_rdy[s]));
           continue;
         }
         const uint4 src = g < 32 ? e0 : e1;
@@ -614,13 +649,6 @@ __global__ void __launch_bounds__(kThreads, 1) expert_kernel(const __grid_consta
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->sfa_rdy[s]));
       }
     }
-    // image copies still in flight land before the CTA may exit
-    if (kFp4 && lane == 0) {
-      for (int s = 0; s < kStages; ++s)
-        if ((walk.touched >> s) & 1u)
-          drain_wait(ptx::smem_u32(&bars->sfa_rdy[s]), walk.last_parity(s));
-    }
-    __syncwarp();
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp - 4;  // TMEM lane quarter
@@ -890,15 +918,17 @@ cudaError_t expert_kernel_setup() {
 cudaError_t expert_occupancy(int fp4, int* per_sm) {
   cudaError_t e = expert_kernel_setup();
   if (e != cudaSuccess) return e;
-  return fp4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, expert_kernel<true>, kThreads,
-                                                             kSmemBytes)
-             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, expert_kernel<false>,
-                                                             kThreads, kSmemBytes);
+  return fp4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                   per_sm, expert_kernel<true>, Roles<true>::kThreads, kSmemBytes)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                   per_sm, expert_kernel<false>, Roles<false>::kThreads, kSmemBytes);
 }
 
 cudaError_t launch_experts(const ExpertParams& p, int grid, cudaStream_t s) {
-  return p.fp4 ? launch_pdl(expert_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, p)
-               : launch_pdl(expert_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+  return p.fp4 ? launch_pdl(expert_kernel<true>, dim3(grid), dim3(Roles<true>::kThreads),
+                            kSmemBytes, s, p)
+               : launch_pdl(expert_kernel<false>, dim3(grid), dim3(Roles<false>::kThreads),
+                            kSmemBytes, s, p);
 }
 
 }  // namespace moe
