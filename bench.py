@@ -5,7 +5,11 @@ Metric: microseconds per MoE decode step, with the achieved HBM GB/s of the
 dominant kernel against the measured copy bandwidth. A step is one pass of the
 whole path (seam, router, top-k with the operand panels, the experts, combine) over one
 batch of M synthetic token rows, replayed from a CUDA graph with every input
-resident in HBM; L2 is flushed (a 512 MB write) before every timed step.
+resident in HBM; L2 is flushed before every timed step: a 512 MB buffer is
+written and then read back, so that L2 holds none of the step's data and no
+dirty lines (a write-only flush leaves ~126 MB of dirty lines that the step
+would write back to HBM while it streams its weights; that time is reported
+beside the headline as us_per_step_after_write_only_flush).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl mine|reference] [--no-sweep]
@@ -75,20 +79,26 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel source and on this workload (else None)."""
+def ncu_traffic(kernel: str, workload: str, alg_bytes: int):
+    """DRAM bytes per launch of `kernel` (dram__bytes_read.sum + write.sum)
+    from the committed ncu summary, if it was taken on the current kernel
+    source (else None). Captured on this workload: the measured bytes;
+    captured on a smaller layer (multi-metric captures stay a few GB on the
+    device): the measured bytes per algorithmic byte there, times this
+    launch's algorithmic bytes. Returns (bytes, how)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
-        return None
+        return None, None
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel)
     if not e or e.get("source_hash") != kernel_hash():
-        return None
-    if str(e.get("workload", "")).split(" ")[0] != workload:
-        return None
-    return e.get("bytes_per_launch")
+        return None, None
+    if e.get("workload") == workload:
+        return e.get("bytes_per_launch"), f"measured on {workload}"
+    ratio = e["bytes_per_launch"] / e["alg_bytes_per_launch"]
+    return round(ratio * alg_bytes), (f"scaled: {ratio:.4f} x the algorithmic bytes, the ratio "
+                                      f"measured on {e['workload']}")
 
 
 class Clocks:
@@ -343,9 +353,16 @@ def run_gpu(args):
     d = wl.dims
     peaks = measured_peaks()
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_sink = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def flush_write_only():
+        flush_buf.fill_(1)
 
     def flush():
+        # write the buffer (evicts the step's data), then read it back: L2 is
+        # left holding clean lines of this buffer only
         flush_buf.fill_(1)
+        flush_sink.copy_(flush_buf.view(torch.int64).sum().view(1))
 
     layer, x, ew = make_layer(wl, dev)
     if world > 1:
@@ -355,6 +372,9 @@ def run_gpu(args):
         step_ms, kmean, unique, graph, out, replay_ms = time_layer(layer, x, dev, args.steps,
                                                                    args.warmup, flush)
     clocks = clk.summary()
+    # the same step after a write-only flush (L2 full of the flush's dirty lines)
+    wo_ms, _, _, _, _, _ = time_layer(layer, x, dev, max(10, args.steps // 4), args.warmup,
+                                      flush_write_only)
     launches_per_step = layer.step_launches(wl.tokens)
     us_step = per_step_us(sum(step_ms), args.steps, world, dev)
     names = kernel_names()
@@ -363,9 +383,11 @@ def run_gpu(args):
     # the expert kernel streams every touched expert (w13 + w2 + their scales) once
     exp_bytes = unique * d.expert_bytes() + d.shared_bytes()
     ach = exp_bytes / (kmean[ix] * 1e-3) / 1e9
+    traffic, traffic_how = ncu_traffic("experts", wl.name, exp_bytes)
     roofline = {"bound": "hbm", "kernel": "experts", "achieved": round(ach, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "traffic": ncu_traffic("experts", wl.name),
+                "traffic": traffic,
+                "traffic_source": traffic_how,
                 "alg_bytes_per_launch": exp_bytes,
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
                 if peaks["source"] == "measured" else "fallback 6.8 TB/s"}
@@ -470,7 +492,9 @@ def run_gpu(args):
                    "step_frac_of_peak": round(step_gbs / peaks["hbm_gbs"], 4) if step_gbs else None,
                    "step_frac_of_8tbs": round(step_gbs / NOMINAL_GBS, 4) if step_gbs else None,
                    "median_us_per_step": round(statistics.median(step_ms) * 1e3, 3),
-                   "l2": "flushed (512 MB write) before every timed step; weights > L2",
+                   "l2": "flushed before every timed step: a 512 MB buffer written, then read "
+                         "back (none of the step's data in L2, no dirty lines); weights > L2",
+                   "us_per_step_after_write_only_flush": round(statistics.mean(wo_ms) * 1e3, 3),
                    "timing": "CUDA-graph replay; the step is timed by event nodes inside its graph "
                              "just before its first kernel and after its last (replay_us_per_step: the "
                              "same graph between stream events, graph launch latency included); "
