@@ -41,6 +41,7 @@ struct moe_handle {
   uint4* sfa2;
   ExpertParams pe;
   int* ready;
+  int* picks_early;  // [1 + kPickPrefetchMaxM * k]: the published-picks count, then the picks
   cudaEvent_t events[16];
   int n_events;
   cudaStream_t last_stream;
@@ -314,6 +315,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   const size_t o_a13 = place(static_cast<size_t>(E + 1) * t13 * g13 * 16);
   const size_t o_a2 = place(static_cast<size_t>(E + 1) * t2 * g2 * 16);
   const size_t o_rd = place(static_cast<size_t>(E + 1) * 4);
+  const size_t o_pk = place(static_cast<size_t>(1 + kPickPrefetchMaxM * K) * 4);
   const bool fp4 = cfg->routed_format == MOE_ROUTED_E2M1;
   // MXFP4 routed experts: per-row scale images, 32 x 16 bytes per (tile, stage)
   const size_t o_i13 = fp4 ? place(static_cast<size_t>(E) * t13 * g13 * 512) : 0;
@@ -345,6 +347,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
   h->sfa13 = reinterpret_cast<uint4*>(b + o_a13);
   h->sfa2 = reinterpret_cast<uint4*>(b + o_a2);
   h->ready = reinterpret_cast<int*>(b + o_rd);
+  h->picks_early = reinterpret_cast<int*>(b + o_pk);
   uint4* img13 = fp4 ? reinterpret_cast<uint4*>(b + o_i13) : nullptr;
   uint4* img2 = fp4 ? reinterpret_cast<uint4*>(b + o_i2) : nullptr;
 
@@ -495,6 +498,10 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   rp.clear_n[1] = h->units_max;
   rp.clear[2] = h->counters + kCtrTasks;
   rp.clear_n[2] = 1;
+  // (small steps with E4M3 routed experts; measured no gain with MXFP4 ones)
+  const bool pick_pf = M <= kPickPrefetchMaxM && h->cfg.routed_format == MOE_ROUTED_E4M3;
+  rp.clear[3] = pick_pf ? h->picks_early : nullptr;  // the published-picks count
+  rp.clear_n[3] = 1;
   // small steps: the last round of w2 tiles runs as K-halves added into the
   // step's partial rows, which start at zero
   const int g2 = h->cfg.inter / 128;
@@ -519,6 +526,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   tp.x8 = h->x8;
   tp.x8c = h->x8c;
   tp.xpan = h->xpan;
+  tp.picks_early = pick_pf ? h->picks_early : nullptr;
   tp.H = H;
   tp.dbg_ids = d.topk_ids;
   tp.dbg_w = d.topk_w;
@@ -552,6 +560,7 @@ int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream
   pe.M = M;
   pe.K = K;
   pe.withhold_unit = h->withhold_unit;
+  pe.picks_early = pick_pf ? h->picks_early : nullptr;
   pe.split_tiles = split ? h->num_sms : 0;
   if (err == cudaSuccess) err = launch_experts(pe, h->num_sms, st);
   mark(4);

@@ -363,6 +363,39 @@ struct SlotWalk {
   __device__ __forceinline__ uint32_t last_parity(int s) const { return parity(s) ^ 1u; }
 };
 
+// Small steps: the top-k kernel publishes each token's picks as soon as it has
+// chosen them, while this grid is already resident and waiting for it. Lane 0
+// of each epilogue warp (idle until the first accumulator is ready) waits for
+// them (bounded, then gives up: only a prefetch is lost) and prefetches into
+// L2 its share -- over every CTA and epilogue warp -- of the picked experts'
+// first kPickPrefetchStages K stages of every w13 tile, the boxes the w13
+// tasks will load first. HBM then streams routed weights while the routing
+// finishes instead of after it.
+__device__ __forceinline__ void prefetch_picks(const ExpertParams& p, int q) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.picks_early) : "memory");
+  if (v < p.M) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (v < p.M) {
+      if (ptx::globaltimer_ns() - t0 > 20000) return;
+      __nanosleep(64);
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.picks_early) : "memory");
+    }
+  }
+  const int n = p.M * p.K;
+  const int S = p.g13 < kPickPrefetchStages ? p.g13 : kPickPrefetchStages;
+  const int items = n * p.t13 * S;
+  for (int it = static_cast<int>(blockIdx.x) * 4 + q; it < items;
+       it += static_cast<int>(gridDim.x) * 4) {
+    const int s = it % S, rest = it / S, t = rest % p.t13, j = rest / p.t13;
+    const int e = __ldcg(p.picks_early + 1 + j);
+    if (e < 0 || e >= p.E) continue;
+    bool seen = false;  // an expert picked by several tokens is prefetched once
+    for (int i = 0; i < j && !seen; ++i) seen = __ldcg(p.picks_early + 1 + i) == e;
+    if (!seen) ptx::prefetch_tensor_3d(&p.tm_w13, s * kStageK, 64 * t, 2 * e);
+  }
+}
+
 // kFp4: the routed experts are MXFP4 (E2M1 with per-row scale images); the
 // E4M3 instantiation carries none of that path's code.
 template <bool kFp4>
@@ -652,6 +685,8 @@ __global__ void __launch_bounds__(Roles<kFp4>::kThreads, 1)
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp - 4;  // TMEM lane quarter
+    if (p.picks_early && lane == 0) prefetch_picks(p, q);
+    __syncwarp();
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [gate | up][n][64]
     int lt = 0;
     for (uint32_t j = 0;; ++j) {

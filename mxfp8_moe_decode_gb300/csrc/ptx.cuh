@@ -145,6 +145,15 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes, uin
                : "memory");
 }
 
+// L2 prefetch of one 3D box of a tensor map (the box a tma_load_3d at these
+// coordinates would copy); no completion to wait for.
+__device__ __forceinline__ void prefetch_tensor_3d(const void* tmap, int32_t x, int32_t y,
+                                                   int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // The same with an L2 cache-eviction policy for the source lines.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar, uint64_t policy) {

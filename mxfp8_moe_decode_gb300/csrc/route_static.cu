@@ -119,7 +119,7 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   rp.dbg_x8 = rp.dbg_x8c = nullptr;
   rp.eps = 0.0f;
   rp.pf_ptr[0] = rp.pf_ptr[1] = nullptr;  // nothing to prefetch
-  for (int r = 0; r < 3; ++r) {  // the memsets above clear the counters
+  for (int r = 0; r < 4; ++r) {  // the memsets above clear the counters
     rp.clear[r] = nullptr;
     rp.clear_n[r] = 0;
   }
@@ -143,6 +143,7 @@ extern "C" int moe_route_static(const void* normed, const void* gate_w, const fl
   tp.x8 = nullptr;
   tp.x8c = nullptr;
   tp.xpan = nullptr;
+  tp.picks_early = nullptr;
   tp.H = hidden;
   tp.dbg_ids = topk_ids;
   tp.dbg_w = topk_w;

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterParams p) 
   ptx::griddep_launch_dependents();
   if (blockIdx.x == 0 && blockIdx.y == 0) {
 #pragma unroll
-    for (int r = 0; r < 3; ++r)
+    for (int r = 0; r < 4; ++r)
       if (p.clear[r])
         for (int i = tid; i < p.clear_n[r]; i += kThreads) p.clear[r][i] = 0;
   }
@@ -403,6 +403,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   }
   __syncthreads();
   if (warp == 0) {
+    // small steps: publish the picks at once (the expert kernel, already
+    // resident, prefetches the picked experts' first stages into L2 while
+    // this grid and its successor's dependency wait finish)
+    if (p.picks_early) {
+      if (lane < K) p.picks_early[1 + m * K + lane] = pick_s[lane];
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.picks_early) : "memory");
+    }
     // the chosen scores' sum in pick order (the same in every lane)
     float ssum = 0.0f;
     bool bad = false;
