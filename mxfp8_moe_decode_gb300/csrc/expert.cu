@@ -819,20 +819,28 @@ __global__ void __launch_bounds__(Roles<kFp4>::kThreads, 1)
       if (pre_ok) st_release_cta(&misc->ready_seq, 0);
     }
     // The routing (row counts) and the routed experts' x panels come from the
-    // top-k kernel: this warp alone waits for it; the other roles wait on the
-    // task queue. The next kernel may start launching now: it waits for this
-    // grid before it reads anything this grid writes, and may read the top-k
-    // kernel's tables at once (that grid is complete).
-    ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
+    // top-k kernel: this warp alone waits for it (in the table's second pass
+    // below); the other roles wait on the task queue. The next kernel may
+    // start launching then: it waits for this grid before it reads anything
+    // this grid writes, and may read the top-k kernel's tables at once (that
+    // grid is complete).
 
     // ---- the step's units (pack_unit) from the per-expert row counts: lane l
     // owns the run of experts l R .. l R + R - 1 (R = ceil(E / 32)); one warp
     // exclusive scan of (rows << 16 | active experts) over the runs gives
     // each active expert its unit index (after the shared expert's 0) and
-    // first row
-    int units;
-    {
+    // first row. Two passes over the same code: the first, before the grid
+    // dependency wait, on counts of zero (no loads, no global writes: its
+    // table is overwritten) so that the instructions are fetched while this
+    // warp would only wait; the second on the top-k kernel's counts.
+    int units = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool real = pass != 0;
+      if (real) {
+        ptx::griddep_wait();
+        ptx::griddep_launch_dependents();
+      }
       const int R = (p.E + 31) >> 5;
       const int e0 = lane * R;
       int n[kMaxExperts / 32];
@@ -840,7 +848,7 @@ __global__ void __launch_bounds__(Roles<kFp4>::kThreads, 1)
       bool bad = false;
 #pragma unroll
       for (int r = 0; r < kMaxExperts / 32; ++r) {
-        n[r] = r < R && e0 + r < p.E ? __ldcg(p.cnt + e0 + r) : 0;
+        n[r] = real && r < R && e0 + r < p.E ? __ldcg(p.cnt + e0 + r) : 0;
         if (n[r] < 0 || n[r] > kMaxTokens) {
           bad = true;
           n[r] = 0;
@@ -858,7 +866,7 @@ __global__ void __launch_bounds__(Roles<kFp4>::kThreads, 1)
       units = routed + 1;
       if (__any_sync(0xffffffffu, bad) || units > p.units_max ||
           static_cast<int>(total >> 16) > p.M * p.K) {
-        if (lane == 0) atomicOr(p.err, kErrBounds);
+        if (real && lane == 0) atomicOr(p.err, kErrBounds);
         units = 0;
       } else {
         const uint32_t excl = incl - mine;
@@ -873,7 +881,7 @@ __global__ void __launch_bounds__(Roles<kFp4>::kThreads, 1)
         if (lane == 0) unit_s[0] = pack_unit(p.E, p.M, p.M * p.K);
       }
       __syncwarp();
-      if (blockIdx.x == 0) {  // the table for diagnostics: routed units, then the shared one
+      if (real && blockIdx.x == 0) {  // the table for diagnostics: routed units, then the shared one
         for (int i = lane; i < units; i += 32) {
           const uint32_t v = unit_s[i];
           p.act[i > 0 ? i - 1 : units - 1] =

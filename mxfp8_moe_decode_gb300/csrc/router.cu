@@ -322,12 +322,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     const int ex = tid + i * kTopkThreads;
     bias[i] = ex < E ? p.bias[ex] : 0.0f;
   }
-  ptx::griddep_wait();  // partial logits come from the router kernel
-  ptx::griddep_launch_dependents();
-
   // this token's MXFP8 row (16-byte pieces) and scale codes (one word per 128
-  // columns), loaded now so that their latency hides behind the selection;
-  // they are stored into the picked experts' panels below
+  // columns), loaded once the grid dependency is met so that their latency
+  // hides behind the selection; they are stored into the picked experts'
+  // panels below
   constexpr int kMaxPieces = 2;  // 16-byte pieces per thread: H <= 8192
   const int H = p.H, G = H >> 7, n16 = H >> 4;
   uint4 xv[kMaxPieces];
@@ -335,110 +333,129 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   // (a lone token's experts read the shared expert's panels, which the seam
   // writes: nothing to store then)
   const bool panels = p.xpan != nullptr && M > 1;
-  if (panels) {
-    const uint4* xrow = reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H);
 #pragma unroll
-    for (int q = 0; q < kMaxPieces; ++q) {
-      const int c = tid + q * kTopkThreads;
-      xv[q] = c < n16 ? __ldcg(xrow + c) : make_uint4(0, 0, 0, 0);
-    }
-    if (tid < G)
-      cw = __ldcg(reinterpret_cast<const uint32_t*>(p.x8c + static_cast<size_t>(m) * (H >> 5)) + tid);
-  }
+  for (int q = 0; q < kMaxPieces; ++q) xv[q] = make_uint4(0, 0, 0, 0);
 
-  // ---- one thread per expert: the KS partials (all loads in flight), then
-  // their sum in a fixed order, the score and the choice key
+  // Two passes over the same code: the first, before the grid dependency
+  // wait, selects on scores of 1/2 (no loads, no global writes) so that the
+  // selection's instructions are fetched while this CTA would only wait; the
+  // second selects on the router's logits.
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool real = pass != 0;
+    if (real) {
+      ptx::griddep_wait();  // partial logits come from the router kernel
+      ptx::griddep_launch_dependents();
+      if (panels) {
+        const uint4* xrow = reinterpret_cast<const uint4*>(p.x8 + static_cast<size_t>(m) * H);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int ex = tid + i * kTopkThreads;
-    if (ex < E) {
-      float part[kMaxKsplit];
-#pragma unroll
-      for (int ks = 0; ks < kMaxKsplit; ++ks)
-        part[ks] = ks < KS ? __ldcg(p.logit_part + (static_cast<size_t>(ks) * M + m) * E + ex) : 0.0f;
-      float logit = 0.0f;
-#pragma unroll
-      for (int ks = 0; ks < kMaxKsplit; ++ks)
-        if (ks < KS) logit += part[ks];
-      const float s = 1.0f / (1.0f + expf(-logit));
-      s_s[ex] = s;
-      key_s[ex] = choice_key(s + bias[i], ex);
-      if (p.dbg_logits) p.dbg_logits[static_cast<size_t>(m) * E + ex] = logit;
-    }
-  }
-  __syncthreads();
-
-  // ---- the k largest keys by rank (keys are distinct: they hold the expert
-  // index): first each expert's rank within its group of 32 (a group's k best
-  // are candidates), then each candidate's rank among all candidates; the
-  // candidate of rank j is pick j
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int ex = tid + i * kTopkThreads;
-    if (ex < E) {
-      const unsigned long long mine = key_s[ex];
-      const unsigned long long* grp = key_s + (ex & ~31);
-      int rank = 0;
-#pragma unroll 8
-      for (int o = 0; o < 32; ++o) rank += grp[o] > mine;
-      if (rank < K) cand_s[(ex >> 5) * K + rank] = mine;
-    }
-  }
-  __syncthreads();
-  // (four adjacent lanes per candidate, each counting over a quarter)
-  const int ncand = (E >> 5) * K;
-  for (int c0 = 0; c0 < ncand; c0 += kTopkThreads / 4) {
-    const int c = c0 + (tid >> 2);
-    const bool live = c < ncand;
-    const unsigned long long mine = live ? cand_s[c] : 0ull;
-    int rank = 0;
-    if (live)
-      for (int o = tid & 3; o < ncand; o += 4) rank += cand_s[o] > mine;
-    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
-    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
-    if (live && (tid & 3) == 0 && rank < K) {
-      const int ex = 0x7fffffff - static_cast<int>(static_cast<uint32_t>(mine));
-      pick_s[rank] = ex;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // small steps: publish the picks at once (the expert kernel, already
-    // resident, prefetches the picked experts' first stages into L2 while
-    // this grid and its successor's dependency wait finish)
-    if (p.picks_early) {
-      if (lane < K) p.picks_early[1 + m * K + lane] = pick_s[lane];
-      __syncwarp();
-      if (lane == 0)
-        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.picks_early) : "memory");
-    }
-    // the chosen scores' sum in pick order (the same in every lane)
-    float ssum = 0.0f;
-    bool bad = false;
-    for (int j = 0; j < K; ++j) {
-      int ex = pick_s[j];
-      if (ex < 0 || ex >= E) {  // only with non-finite scores
-        bad = true;
-        ex = 0;
+        for (int q = 0; q < kMaxPieces; ++q) {
+          const int c = tid + q * kTopkThreads;
+          xv[q] = c < n16 ? __ldcg(xrow + c) : make_uint4(0, 0, 0, 0);
+        }
+        if (tid < G)
+          cw = __ldcg(reinterpret_cast<const uint32_t*>(p.x8c + static_cast<size_t>(m) * (H >> 5)) +
+                      tid);
       }
-      ssum += s_s[ex];
     }
-    if (bad && lane == 0) atomicOr(&p.counters[kCtrErr], kErrBounds);
-    if (lane < K) {
-      int my_id = pick_s[lane];
-      if (my_id < 0 || my_id >= E) my_id = 0;
-      pk_w = s_s[my_id] / ssum;
-      // the token's row among the expert's rows this step (any order: an MMA
-      // output column depends on its own row only); a lone token's is row 0
-      pk_slot = M > 1 ? atomicAdd(p.cnt + my_id, 1) : 0;
-      pk_id = my_id;
-      pick_s[lane] = my_id;
-      slot_s[lane] = pk_slot;
+
+    // ---- one thread per expert: the KS partials (all loads in flight), then
+    // their sum in a fixed order, the score and the choice key
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int ex = tid + i * kTopkThreads;
+      if (ex < E) {
+        float logit = 0.0f;
+        if (real) {
+          float part[kMaxKsplit];
+#pragma unroll
+          for (int ks = 0; ks < kMaxKsplit; ++ks)
+            part[ks] =
+                ks < KS ? __ldcg(p.logit_part + (static_cast<size_t>(ks) * M + m) * E + ex) : 0.0f;
+#pragma unroll
+          for (int ks = 0; ks < kMaxKsplit; ++ks)
+            if (ks < KS) logit += part[ks];
+        }
+        const float s = 1.0f / (1.0f + expf(-logit));
+        s_s[ex] = s;
+        key_s[ex] = choice_key(s + bias[i], ex);
+        if (real && p.dbg_logits) p.dbg_logits[static_cast<size_t>(m) * E + ex] = logit;
+      }
     }
+    __syncthreads();
+
+    // ---- the k largest keys by rank (keys are distinct: they hold the expert
+    // index): first each expert's rank within its group of 32 (a group's k best
+    // are candidates), then each candidate's rank among all candidates; the
+    // candidate of rank j is pick j
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int ex = tid + i * kTopkThreads;
+      if (ex < E) {
+        const unsigned long long mine = key_s[ex];
+        const unsigned long long* grp = key_s + (ex & ~31);
+        int rank = 0;
+#pragma unroll 8
+        for (int o = 0; o < 32; ++o) rank += grp[o] > mine;
+        if (rank < K) cand_s[(ex >> 5) * K + rank] = mine;
+      }
+    }
+    __syncthreads();
+    // (four adjacent lanes per candidate, each counting over a quarter)
+    const int ncand = (E >> 5) * K;
+    for (int c0 = 0; c0 < ncand; c0 += kTopkThreads / 4) {
+      const int c = c0 + (tid >> 2);
+      const bool live = c < ncand;
+      const unsigned long long mine = live ? cand_s[c] : 0ull;
+      int rank = 0;
+      if (live)
+        for (int o = tid & 3; o < ncand; o += 4) rank += cand_s[o] > mine;
+      rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+      rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+      if (live && (tid & 3) == 0 && rank < K) {
+        const int ex = 0x7fffffff - static_cast<int>(static_cast<uint32_t>(mine));
+        pick_s[rank] = ex;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // small steps: publish the picks at once (the expert kernel, already
+      // resident, prefetches the picked experts' first stages into L2 while
+      // this grid and its successor's dependency wait finish)
+      if (real && p.picks_early) {
+        if (lane < K) p.picks_early[1 + m * K + lane] = pick_s[lane];
+        __syncwarp();
+        if (lane == 0)
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.picks_early) : "memory");
+      }
+      // the chosen scores' sum in pick order (the same in every lane)
+      float ssum = 0.0f;
+      bool bad = false;
+      for (int j = 0; j < K; ++j) {
+        int ex = pick_s[j];
+        if (ex < 0 || ex >= E) {  // only with non-finite scores
+          bad = true;
+          ex = 0;
+        }
+        ssum += s_s[ex];
+      }
+      if (real && bad && lane == 0) atomicOr(&p.counters[kCtrErr], kErrBounds);
+      if (lane < K) {
+        int my_id = pick_s[lane];
+        if (my_id < 0 || my_id >= E) my_id = 0;
+        pk_w = s_s[my_id] / ssum;
+        // the token's row among the expert's rows this step (any order: an MMA
+        // output column depends on its own row only); a lone token's is row 0
+        pk_slot = real && M > 1 ? atomicAdd(p.cnt + my_id, 1) : 0;
+        pk_id = my_id;
+        pick_s[lane] = my_id;
+        slot_s[lane] = pk_slot;
+      }
+    }
+    // (global stores go after the barriers where they can: a block barrier
+    // waits for the stores before it)
+    __syncthreads();
   }
-  // (global stores go after the barriers where they can: a block barrier
-  // waits for the stores before it)
-  __syncthreads();
 
   // ---- this token's MXFP8 row and codes into the x panels of its experts
   // (row = its slot): each 16-byte piece is read once and stored k times.
