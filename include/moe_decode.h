@@ -175,16 +175,20 @@ int moe_create(const moe_config* cfg, const moe_weights* w, int device, moe_hand
  * them on one stream). Errors are checked before anything is enqueued:
  * MOE_ERR_RANGE (M < 1 or M > max_tokens), MOE_ERR_ARG, MOE_ERR_ALIGN,
  * MOE_ERR_CUDA (a launch failed). A device-side failure (a bounded wait that
- * expired) is reported later by moe_status.
+ * expired) is reported later by moe_status. A row holding NaN or infinite
+ * values is routed to k distinct valid experts and raises no error; its own
+ * output row is unspecified, every other row is as without it.
  */
 int moe_decode_step(moe_handle* h, const void* x, int M, void* out, void* stream,
                     const moe_debug* dbg);
 
 /*
  * Synchronises the handle's device and returns MOE_OK, MOE_ERR_TIMEOUT if a
- * step's kernel gave up a bounded wait since the last moe_clear_status, or
- * MOE_ERR_CUDA if the device reported an error. Not allowed during capture
- * (MOE_ERR_CAPTURE).
+ * step's kernel gave up a bounded wait since the last moe_clear_status,
+ * MOE_ERR_ARG if a kernel found a pick or a per-expert row count out of range
+ * (a defensive check: top-k always picks k distinct valid experts, even from
+ * non-finite scores, so only corrupted scratch sets it), or MOE_ERR_CUDA if
+ * the device reported an error. Not allowed during capture (MOE_ERR_CAPTURE).
  */
 int moe_status(moe_handle* h);
 
@@ -319,7 +323,8 @@ void moe_destroy(moe_handle* h);
  *
  * Device-side errors are not returned by the call (it only enqueues): read
  * them with moe_route_static_status. Rows whose scores are not finite (NaN or
- * infinite inputs) give unspecified ids and NaN weights and no error.
+ * infinite inputs) give k distinct valid but unspecified ids and NaN weights,
+ * and no error.
  */
 #define MOE_ROUTE_STATIC_SCRATCH_BYTES (256 * 1024)
 int moe_route_static(const void* normed, const void* gate_w, const float* bias, int M,

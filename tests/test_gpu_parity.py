@@ -92,6 +92,30 @@ def test_tiny_special_rows(tiny):
     assert np.all(np.isfinite(f64(out)))
 
 
+@pytest.mark.parametrize("m", [3, 6])  # the seam fused into the router, and its own kernel
+def test_tiny_nonfinite_rows_stay_in_their_rows(tiny, m):
+    # A NaN row and a row with one infinite element: the choice keys are
+    # integers made from the scores' bits and the expert index, so top-k
+    # still picks k distinct valid experts for them, nothing reads or writes
+    # out of bounds, and no error is raised. Every token's output depends on
+    # its own row only, so the finite rows must still match the oracle run on
+    # those rows alone.
+    x, _ = gapped_tokens(tiny.wl, tiny.ri, m=m)
+    x[1] = float("nan")
+    x[m - 1, 5] = float("inf")
+    out, dbg = tiny.run(x)
+    assert tiny.layer.status() == 0
+    d = tiny.wl.dims
+    ids = dbg["topk_ids"].numpy()
+    for r in (1, m - 1):
+        assert len(set(ids[r].tolist())) == d.topk and ids[r].min() >= 0 and ids[r].max() < d.experts
+    rows = [r for r in range(m) if r not in (1, m - 1)]
+    ref = tiny.oracle(x[rows])
+    assert np.array_equal(ids[rows], ref.routing.ids)
+    assert rel_err(f64(out)[rows], ref.out) <= OUT_TOL
+    assert np.all(np.isfinite(f64(out)[rows]))
+
+
 def test_tiny_deterministic_and_graph(tiny):
     x, _ = gapped_tokens(tiny.wl, tiny.ri, m=5)
     xd = x.to(tiny.dev)
