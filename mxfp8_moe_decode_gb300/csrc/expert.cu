@@ -369,8 +369,8 @@ struct SlotWalk {
 // them (bounded, then gives up: only a prefetch is lost) and prefetches into
 // L2 its share -- over every CTA and epilogue warp -- of the picked experts'
 // first kPickPrefetchStages K stages of every w13 tile, the boxes the w13
-// tasks will load first. HBM then streams routed weights while the routing
-// finishes instead of after it.
+// tasks will load first, and of their compact weight-scale entries. HBM then
+// streams routed weights while the routing finishes instead of after it.
 __device__ __forceinline__ void prefetch_picks(const ExpertParams& p, int q) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.picks_early) : "memory");
@@ -393,6 +393,23 @@ __device__ __forceinline__ void prefetch_picks(const ExpertParams& p, int q) {
     bool seen = false;  // an expert picked by several tokens is prefetched once
     for (int i = 0; i < j && !seen; ++i) seen = __ldcg(p.picks_early + 1 + i) == e;
     if (!seen) ptx::prefetch_tensor_3d(&p.tm_w13, s * kStageK, 64 * t, 2 * e);
+  }
+  // every picked expert's compact weight-scale entries (w13 and w2: one
+  // contiguous range each), which the scale-image warp loads at each task's
+  // start (with the weights' boxes, an HBM round trip before the first MMA of
+  // a tile; on one GB300: M=1 -1.6 us, the 384-expert layer at M=1 -0.4 us):
+  // pick j from CTA j
+  const int j = static_cast<int>(blockIdx.x);
+  if (q == 0 && j < n) {
+    const int e = __ldcg(p.picks_early + 1 + j);
+    bool seen = e < 0 || e >= p.E;
+    for (int i = 0; i < j && !seen; ++i) seen = __ldcg(p.picks_early + 1 + i) == e;
+    if (!seen) {
+      const uint64_t pol = ptx::policy_evict_normal();
+      const size_t n13 = static_cast<size_t>(p.t13) * p.g13, n2 = static_cast<size_t>(p.t2) * p.g2;
+      ptx::prefetch_l2(p.sfa13 + e * n13, static_cast<uint32_t>(n13 * 16), pol);
+      ptx::prefetch_l2(p.sfa2 + e * n2, static_cast<uint32_t>(n2 * 16), pol);
+    }
   }
 }
 
