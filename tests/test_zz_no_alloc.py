@@ -96,6 +96,54 @@ def test_route_static_full_size_router():
         np.testing.assert_allclose(wts, rt.weights[:m], rtol=W_RTOL)
 
 
+def test_route_static_in_a_cuda_graph():
+    # The call's scratch is the library's fixed array, so it can be captured:
+    # captured once and replayed, it gives the uncaptured call's ids and
+    # weights bit for bit; its status call refuses while the stream captures
+    # (it would have to synchronise), and so does a layer's.
+    wl = W.WORKLOADS["full_m16"]
+    d = wl.dims
+    dev = torch.device("cuda:0")
+    ri = W.router_inputs(wl)
+    x, _ = gapped_tokens(wl, ri)
+    normed64 = O.rmsnorm(f64(x), f64(ri["norm_w"]), d.eps)
+    normed = torch.from_numpy(normed64).to(torch.bfloat16).to(dev)
+    gate_w = ri["gate_w"].to(dev)
+    bias = ri["bias"].to(dev)
+    m = normed.shape[0]
+    ids0, wts0 = _route(normed, gate_w, bias, d.topk, dev)  # outside capture first
+
+    ids = torch.full((m, d.topk), -1, dtype=torch.int32, device=dev)
+    wts = torch.full((m, d.topk), -1.0, dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    L = Layer(W.WORKLOADS["tiny_m1"])
+    try:
+        xt = gapped_tokens(L.wl, L.ri, m=2)[0].to(dev)
+        with torch.cuda.stream(s):
+            L.layer.step(xt, stream=s)  # the layer's last stream is s
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                rc = _lib.lib().moe_route_static(normed.data_ptr(), gate_w.data_ptr(), bias.data_ptr(),
+                                                 m, d.hidden, d.experts, d.topk, ids.data_ptr(),
+                                                 wts.data_ptr(), ctypes.c_void_p(s.cuda_stream))
+                st = _lib.lib().moe_route_static_status(ctypes.c_void_p(s.cuda_stream))
+                layer_st = L.layer.status()
+        assert rc == _lib.MOE_OK, rc
+        assert st == _lib.MOE_ERR_CAPTURE, st
+        assert layer_st == _lib.MOE_ERR_CAPTURE, layer_st
+        assert torch.all(ids == -1)  # nothing ran during capture
+        g.replay()
+        torch.cuda.synchronize(dev)
+        assert np.array_equal(ids.cpu().numpy(), ids0)
+        assert np.array_equal(wts.cpu().numpy(), wts0)  # bit for bit
+        assert _lib.lib().moe_route_static_status(ctypes.c_void_p(s.cuda_stream)) == _lib.MOE_OK
+        assert L.layer.status() == _lib.MOE_OK
+    finally:
+        L.close()
+
+
 def test_route_static_refuses_oversized_and_bad_args():
     fn = _lib.lib().moe_route_static
     p = 0x10000  # never dereferenced: every call below is refused on the host
