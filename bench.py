@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -72,10 +73,15 @@ NOMINAL_GBS = 8000.0  # GB300 HBM3e nominal bandwidth: the metric's "% of 8 TB/s
 
 
 def kernel_hash() -> str:
+    """Hash of the expert kernel's sources without comments and whitespace
+    (an edit of a comment leaves the kernel, and its counters, as they were)."""
     h = hashlib.sha256()
     for f in ("expert.cu", "ptx.cuh", "mx.cuh", "internal.cuh"):
-        with open(os.path.join(ROOT, "mxfp8_moe_decode_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "mxfp8_moe_decode_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)  # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

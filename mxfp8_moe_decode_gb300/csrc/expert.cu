@@ -256,8 +256,8 @@ __device__ __forceinline__ bool wait_ready(const int* ctr, int target, volatile 
 }
 
 // The j-th task of this CTA: the scheduler posts its id (-1: no more tasks)
-// with its unit's table entry; each of the five readers takes both and frees
-// the slot at once. A reader gets -2 when a wait gave up (the abort flag is set).
+// with its unit's table entry; each reader (the producers, the issuers, the
+// scale-image warp and the epilogue) takes both and frees the slot at once. A reader gets -2 when a wait gave up (the abort flag is set).
 // A decoded task in 16 bytes: phase, half and tile; unit; first stage and
 // stage count.
 __device__ __forceinline__ int4 pack_task(const Task& k) {
